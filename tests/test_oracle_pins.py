@@ -1,0 +1,302 @@
+"""Pins for the fp64 oracle: each checks it against something other than itself.
+
+* a hand-decoded worked example of the storage (tests/golden),
+* single-hot brute force on every block size (pins the (n, k) -> byte/nibble map),
+* a second reading of the layout, from the fp16 GEMV kernel's 32-bit word loads,
+* exact rational brute force on a tiny problem,
+* the integer special case (zp 0, scale 1, integer activations) against int64 matmul,
+* invariants: all codes equal to the zero point give Y = 0; scale linearity;
+  the default zero point 8 equals an explicit 0x88 buffer,
+* fp16 decoding against numpy's own conversion for all 65536 bit patterns,
+* silu against ``x * scipy.special.expit(x)``,
+* the repacked layout: a hand-placed code, and the round trip.
+"""
+from __future__ import annotations
+
+import fractions
+import os
+
+import numpy as np
+import pytest
+
+import mnb_synth as syn
+from oracle import mnb_oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "layout_worked_example.txt")
+
+
+def _read_golden(path):
+    out = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            out[key] = vals
+    return out
+
+
+def _pack_codes(codes_nk: np.ndarray) -> np.ndarray:
+    """Test-side packer (the inverse direction): row n is K/2 bytes, low nibble = even k."""
+    N, K = codes_nk.shape
+    c = codes_nk.astype(np.uint8)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def _pack_zp(zp_ng: np.ndarray) -> np.ndarray:
+    N, G = zp_ng.shape
+    zrb = -(-G // 2)
+    out = np.zeros((N, zrb), dtype=np.uint8)
+    for g in range(G):
+        if g % 2 == 0:
+            out[:, g // 2] |= zp_ng[:, g].astype(np.uint8)
+        else:
+            out[:, g // 2] |= (zp_ng[:, g].astype(np.uint8) << 4)
+    return out
+
+
+def test_golden_worked_example():
+    g = _read_golden(GOLDEN)
+    K, N, bs = int(g["K"][0]), int(g["N"][0]), int(g["block_size"][0])
+    packed = np.array([int(x, 16) for x in g["packed"]], dtype=np.uint8).reshape(N, -1)
+    zp = np.array([int(x, 16) for x in g["zero_points"]], dtype=np.uint8).reshape(N, -1)
+    scales = np.array([int(x, 16) for x in g["scales_f16_bits"]], dtype=np.uint16).view(np.float16).reshape(N, -1)
+    W = orc.dequant_kn_f32(packed, scales, zp, K, N, bs)
+    np.testing.assert_array_equal(W[:, 0], np.array(g["dequant_n0"], dtype=np.float32))
+    np.testing.assert_array_equal(W[:, 1], np.array(g["dequant_n1"], dtype=np.float32))
+    A = np.ones((1, K), dtype=np.float16)
+    Y, B = orc.matmul(A, packed, scales, zp, K, N, bs)
+    np.testing.assert_array_equal(Y[0], np.array(g["y_ones"], dtype=np.float64))
+    np.testing.assert_array_equal(B[0], np.array(g["bound_ones"], dtype=np.float64))
+    Y0, _ = orc.matmul(A, packed, scales, None, K, N, bs)
+    np.testing.assert_array_equal(Y0[0], np.array(g["y_ones_no_zp"], dtype=np.float64))
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+def test_single_hot_layout(bs):
+    """One code differs from the zero point; A = e_k: only Y[n] is nonzero, exactly."""
+    K, N = 3 * bs, 5
+    G = K // bs
+    rng = np.random.default_rng(bs)
+    scales = (rng.uniform(0.25, 2.0, size=(N, G))).astype(np.float16)
+    for (n, k, c) in [(0, 0, 3), (1, 1, 15), (4, K - 1, 0), (2, bs + 1, 12), (3, 2 * bs, 9)]:
+        packed = np.full((N, K // 2), 0x88, dtype=np.uint8)   # every code 8 = default zp
+        byte = n * (K // 2) + k // 2
+        flat = packed.reshape(-1)
+        flat[byte] = (flat[byte] & 0xF0) | c if k % 2 == 0 else (flat[byte] & 0x0F) | (c << 4)
+        A = np.zeros((1, K), dtype=np.float16)
+        A[0, k] = 1.0
+        Y, B = orc.matmul(A, packed, scales, None, K, N, bs)
+        expect = np.zeros(N)
+        expect[n] = (c - 8) * float(scales[n, k // bs])
+        np.testing.assert_array_equal(Y[0], expect)
+        W = orc.dequant_kn_f32(packed, scales, None, K, N, bs)
+        assert np.count_nonzero(W) == (1 if c != 8 else 0)
+        assert W[k, n] == np.float32(expect[n])
+
+
+@pytest.mark.parametrize("g", [0, 1, 2, 5])
+def test_zero_point_nibble_order(g):
+    """A single non-default zero point at an even or odd group shifts only that group."""
+    bs, G, N = 16, 6, 3
+    K = bs * G
+    zp_ng = np.full((N, G), 8)
+    zp_ng[1, g] = 3
+    zp = _pack_zp(zp_ng)
+    packed = np.full((N, K // 2), 0x88, dtype=np.uint8)
+    scales = np.ones((N, G), dtype=np.float16)
+    W = orc.dequant_kn_f32(packed, scales, zp, K, N, bs)
+    expect = np.zeros((K, N), dtype=np.float32)
+    expect[g * bs:(g + 1) * bs, 1] = 8 - 3
+    np.testing.assert_array_equal(W, expect)
+    # explicit nibble check by byte: low nibble for even g
+    byte = zp[1, g // 2]
+    assert ((byte & 15) if g % 2 == 0 else (byte >> 4)) == 3
+
+
+def test_layout_second_reading_u32_words():
+    """The fp16 GEMV kernel in matmul_nbits.rs loads aligned 32-bit words of a row and
+    takes nibble i (bits 4i..4i+3) as k = depth + i.  Decoding that way must agree."""
+    K, N, bs = 256, 7, 32
+    packed = syn.random_bytes(1234, N * K // 2).reshape(N, K // 2)
+    words = packed.reshape(-1).view("<u4").reshape(N, K // 8).astype(np.int64)
+    by_words = np.empty((N, K), dtype=np.int64)
+    for i in range(8):
+        by_words[:, i::8] = (words >> (4 * i)) & 15
+    np.testing.assert_array_equal(orc.codes(packed, K, N, bs), by_words)
+
+
+def test_default_zero_point_is_8():
+    wl = syn.custom("pin_default_zp", 3, 192, 40, 64, has_zp=False)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    explicit = np.full((wl.N, wl.zp_row_bytes), 0x88, dtype=np.uint8)
+    Y0, B0 = orc.matmul(A, w.packed, w.scales, None, wl.K, wl.N, wl.block_size)
+    Y1, B1 = orc.matmul(A, w.packed, w.scales, explicit, wl.K, wl.N, wl.block_size)
+    np.testing.assert_array_equal(Y0, Y1)
+    np.testing.assert_array_equal(B0, B1)
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+def test_all_codes_equal_zero_point_gives_zero(bs):
+    K, N, M = 2 * bs, 9, 3
+    G = K // bs
+    rng = np.random.default_rng(7 + bs)
+    zp_ng = rng.integers(0, 16, size=(N, G))
+    codes_nk = np.repeat(zp_ng, bs, axis=1)
+    packed = _pack_codes(codes_nk)
+    zp = _pack_zp(zp_ng)
+    scales = rng.uniform(0.001, 3.0, size=(N, G)).astype(np.float32)
+    A = rng.standard_normal((M, K)).astype(np.float16)
+    Y, B = orc.matmul(A, packed, scales, zp, K, N, bs)
+    assert np.all(Y == 0.0) and np.all(B == 0.0)
+
+
+def test_scale_linearity():
+    """Doubling one group's scale doubles exactly that group's contribution."""
+    wl = syn.custom("pin_linearity", 1, 128, 6, 32, scales_dtype="f16")
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    g = 2
+    A_in = np.zeros_like(A)
+    A_in[:, g * 32:(g + 1) * 32] = A[:, g * 32:(g + 1) * 32]
+    A_out = A - A_in
+    s2 = w.scales.copy()
+    s2[:, g] = (s2[:, g].astype(np.float32) * 2).astype(np.float16)  # power of two: exact
+    y_in, _ = orc.matmul(A_in, w.packed, w.scales, w.zero_points, wl.K, wl.N, 32)
+    y_in2, _ = orc.matmul(A_in, w.packed, s2, w.zero_points, wl.K, wl.N, 32)
+    y_out, _ = orc.matmul(A_out, w.packed, w.scales, w.zero_points, wl.K, wl.N, 32)
+    y_out2, _ = orc.matmul(A_out, w.packed, s2, w.zero_points, wl.K, wl.N, 32)
+    np.testing.assert_array_equal(y_in2, 2 * y_in)
+    np.testing.assert_array_equal(y_out2, y_out)
+
+
+def test_integer_special_case_matches_int64_matmul():
+    """zp = 0, scale = 1, integer activations: Y is the integer product of A and the codes."""
+    K, N, M, bs = 256, 33, 4, 64
+    G = K // bs
+    rng = np.random.default_rng(99)
+    codes_nk = rng.integers(0, 16, size=(N, K))
+    packed = _pack_codes(codes_nk)
+    zp = np.zeros((N, -(-G // 2)), dtype=np.uint8)
+    scales = np.ones((N, G), dtype=np.float16)
+    A_int = rng.integers(-8, 9, size=(M, K))
+    Y, B = orc.matmul(A_int.astype(np.float16), packed, scales, zp, K, N, bs)
+    exact = A_int.astype(np.int64) @ codes_nk.astype(np.int64).T
+    np.testing.assert_array_equal(Y, exact.astype(np.float64))
+    np.testing.assert_array_equal(B, (np.abs(A_int) @ codes_nk.T).astype(np.float64))
+
+
+def test_exact_rational_brute_force():
+    """Tiny problem in exact rationals, decoding bytes the word way, summing in any order."""
+    wl = syn.custom("pin_rational", 2, 64, 3, 16, scales_dtype="f32")
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    K, N, bs, G = wl.K, wl.N, wl.block_size, wl.k_blocks
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
+    for m in range(wl.M):
+        for n in range(N):
+            acc = fractions.Fraction(0)
+            row = w.packed[n].tobytes()
+            for k in range(K):
+                b = row[k // 2]
+                code = (b >> 4) if k % 2 else (b & 15)
+                zb = int(w.zero_points[n][(k // bs) // 2])
+                zpv = (zb >> 4) if (k // bs) % 2 else (zb & 15)
+                s = fractions.Fraction(float(w.scales[n, k // bs]))
+                a = fractions.Fraction(float(A[m, k]))
+                acc += a * (code - zpv) * s
+            assert abs(Y[m, n] - float(acc)) <= 1e-12 * max(1.0, B[m, n])
+
+
+def test_f16_decode_all_bit_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = orc.f16_to_f64(bits.view(np.float16))
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    np.testing.assert_array_equal(ours[~nan], ref[~nan])
+
+
+def test_silu_against_expit():
+    scipy_special = pytest.importorskip("scipy.special")
+    x = np.linspace(-40, 40, 2001)
+    np.testing.assert_allclose(orc.silu(x), x * scipy_special.expit(x), rtol=1e-14, atol=1e-300)
+    assert orc.silu(np.array([0.0]))[0] == 0.0
+
+
+def test_dequant_matches_product_definition():
+    """Y equals A times the fp32 dequantised matrix when that matrix is exact (fp16 scales)."""
+    wl = syn.custom("pin_compose", 3, 256, 20, 32, scales_dtype="f16")
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    W = orc.dequant_kn_f32(w.packed, w.scales, w.zero_points, wl.K, wl.N, 32).astype(np.float64)
+    Y, _ = orc.matmul(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, 32)
+    np.testing.assert_allclose(orc.activations_f64(A) @ W, Y, rtol=0, atol=1e-12)
+
+
+def test_partial_last_block():
+    """K not a multiple of bs: k_blocks = ceil(K/bs); padding nibbles are never read."""
+    K, N, bs = 40, 2, 16          # 3 blocks, the last one half used
+    G = 3
+    rng = np.random.default_rng(5)
+    packed = rng.integers(0, 256, size=(N, G * bs // 2)).astype(np.uint8)
+    scales = np.ones((N, G), dtype=np.float16)
+    c = orc.codes(packed, K, N, bs)
+    assert c.shape == (N, K)
+    # k = 32..39 live in block 2, bytes 16..19 of the row's 24
+    np.testing.assert_array_equal(c[:, 32], packed[:, 16] & 15)
+    np.testing.assert_array_equal(c[:, 39], packed[:, 19] >> 4)
+    W = orc.dequant_kn_f32(packed, scales, None, K, N, bs)
+    assert W.shape == (K, N)
+
+
+def test_repack_hand_placed_code():
+    """Code 7 at (n=1, k=3) lands in byte 18, high nibble (hand-derived from the layout).
+
+    Tile 0, k-block 0, q = 0, r = 1 -> offset 16; i = 3 = 8*0 + 2*(p%4) + p//4 gives
+    p = 5: word 0, byte 5//2 = 2, odd p -> high nibble.  Offset 16 + 2 = 18.
+    """
+    K, N, bs = 64, 2, 32
+    codes_nk = np.zeros((N, K), dtype=np.int64)
+    codes_nk[1, 3] = 7
+    out = orc.repack(_pack_codes(codes_nk), K, N, bs)
+    assert out.size == 128 * 64 // 2
+    nz = np.nonzero(out)[0]
+    assert list(nz) == [18] and out[18] == 0x70
+    # and (n=130, k=70): tile 1, k-block 1 of Kp/64 = 2 -> block 3 at 12288; q = 0, r = 2,
+    # i = 6 = 2*(p%4) + p//4 -> p = 3: byte 1, high nibble.  12288 + 32 + 1 = 12321.
+    K, N = 128, 131
+    codes_nk = np.zeros((N, K), dtype=np.int64)
+    codes_nk[130, 70] = 5
+    out = orc.repack(_pack_codes(codes_nk), K, N, 64)
+    assert out.size == 256 * 128 // 2
+    nz = np.nonzero(out)[0]
+    assert list(nz) == [12321] and out[12321] == 0x50
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+def test_repack_roundtrip_is_bijection(bs):
+    K, N = 3 * max(bs, 64), 5 + 128
+    packed = syn.random_bytes(77 + bs, N * K // 2).reshape(N, K // 2)
+    rp = orc.repack(packed, K, N, bs)
+    assert rp.size == orc.repacked_bytes(K, N)
+    np.testing.assert_array_equal(orc.unrepack_codes(rp, K, N), orc.codes(packed, K, N, bs))
+    # every stored nibble used exactly once; padding nibbles are zero
+    byte, half = orc._repack_positions(K, N)
+    slots = byte * 2 + half
+    assert np.unique(slots).size == slots.size
+    mask = np.ones(rp.size * 2, dtype=bool)
+    mask[slots.reshape(-1)] = False
+    nibbles = np.stack([rp & 15, rp >> 4], axis=1).reshape(-1)
+    assert np.all(nibbles[mask] == 0)
+
+
+def test_synth_streams_are_deterministic():
+    a = syn.splitmix64(42, 5)
+    b = syn.splitmix64(42, 5)
+    assert np.array_equal(a, b)
+    # SplitMix64 reference outputs for seed 0 (first three values of the published generator)
+    z = syn.splitmix64(0, 3)
+    assert [int(x) for x in z] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
