@@ -1,0 +1,219 @@
+"""Python binding of libmnb (block-quantized INT4 MatMulNBits GEMV/GEMM for sm_103a).
+
+Argument marshalling only: every entry point forwards raw device pointers, sizes and
+the current CUDA stream to the C ABI declared in ``include/mnb.h``; all arithmetic runs
+in the library's CUDA kernels.  PyTorch supplies device memory and streams.  When an
+output tensor is not passed, the binding allocates it with torch before the call (pass
+``out=`` to keep a call free of allocations, e.g. under CUDA-graph capture).
+
+The names match the C entry points: ``mnb_dequant``, ``mnb_repacked_bytes``,
+``mnb_repack``, ``mnb_gemv``, ``mnb_workspace_bytes``, ``mnb_gemm``,
+``mnb_gemv_gate_up_swiglu``, ``mnb_set_programmatic_launch``, ``mnb_last_error``,
+``mnb_last_variant``, ``mnb_version``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmnb.so")
+
+MNB_OK, MNB_ERR_INVALID_ARG, MNB_ERR_UNSUPPORTED, MNB_ERR_MISALIGNED = 0, 1, 2, 3
+MNB_ERR_CAPTURE, MNB_ERR_CUDA, MNB_ERR_TIMEOUT = 4, 5, 6
+MNB_F16, MNB_F32 = 0, 1
+STATUS_NAMES = {0: "MNB_OK", 1: "MNB_ERR_INVALID_ARG", 2: "MNB_ERR_UNSUPPORTED",
+                3: "MNB_ERR_MISALIGNED", 4: "MNB_ERR_CAPTURE", 5: "MNB_ERR_CUDA",
+                6: "MNB_ERR_TIMEOUT"}
+
+
+class MnbError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class MnbWeight(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("scales_dtype", ctypes.c_int32), ("zero_points", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libmnb.so (built in-tree by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m gemm_mnb_gemv_gb300._build` "
+                          "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    c_int, c_size, vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+    sigs = {
+        "mnb_dequant": (c_int, [MnbWeight, c_int, c_int, c_int, vp, vp]),
+        "mnb_repacked_bytes": (c_size, [c_int, c_int, c_int]),
+        "mnb_repack": (c_int, [vp, c_int, c_int, c_int, vp, vp]),
+        "mnb_gemv": (c_int, [vp, MnbWeight, c_int, c_int, c_int, vp, vp]),
+        "mnb_workspace_bytes": (c_size, [c_int, c_int, c_int, c_int]),
+        "mnb_gemm": (c_int, [vp, c_int, MnbWeight, vp, c_int, c_int, c_int, vp, c_size, vp, vp]),
+        "mnb_gemv_gate_up_swiglu": (c_int, [vp, MnbWeight, MnbWeight, c_int, c_int, c_int, vp, vp]),
+        "mnb_set_programmatic_launch": (None, [c_int]),
+        "mnb_last_error": (ctypes.c_char_p, []),
+        "mnb_last_variant": (ctypes.c_char_p, []),
+        "mnb_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_dev(name, t, dtype=None):
+    torch = _torch()
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _weight(packed, scales, zero_points) -> MnbWeight:
+    torch = _torch()
+    _check_dev("packed", packed, torch.uint8)
+    _check_dev("scales", scales)
+    _check_dev("zero_points", zero_points, torch.uint8)
+    if scales.dtype == torch.float16:
+        sd = MNB_F16
+    elif scales.dtype == torch.float32:
+        sd = MNB_F32
+    else:
+        raise TypeError("scales must be float16 or float32")
+    return MnbWeight(packed.data_ptr(), scales.data_ptr(), sd,
+                     zero_points.data_ptr() if zero_points is not None else None)
+
+
+def _raise(status: int):
+    if status != MNB_OK:
+        raise MnbError(status, load_library().mnb_last_error().decode())
+
+
+def mnb_last_error() -> str:
+    return load_library().mnb_last_error().decode()
+
+
+def mnb_last_variant() -> str:
+    return load_library().mnb_last_variant().decode()
+
+
+def mnb_version() -> str:
+    return load_library().mnb_version().decode()
+
+
+def mnb_set_programmatic_launch(enable: bool) -> None:
+    load_library().mnb_set_programmatic_launch(1 if enable else 0)
+
+
+def mnb_repacked_bytes(K: int, N: int, block_size: int) -> int:
+    return int(load_library().mnb_repacked_bytes(K, N, block_size))
+
+
+def mnb_workspace_bytes(M: int, K: int, N: int, block_size: int) -> int:
+    return int(load_library().mnb_workspace_bytes(M, K, N, block_size))
+
+
+def mnb_dequant(packed, scales, zero_points, K: int, N: int, block_size: int, out=None, stream=None):
+    """fp32 ``[K, N]`` dequantised weight (``out[k, n] = (code - zp) * scale``)."""
+    torch = _torch()
+    lib = load_library()
+    w = _weight(packed, scales, zero_points)
+    if out is None:
+        out = torch.empty((K, N), dtype=torch.float32, device=packed.device)
+    _check_dev("out", out, torch.float32)
+    _raise(lib.mnb_dequant(w, K, N, block_size, _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def mnb_repack(packed, K: int, N: int, block_size: int, out=None, stream=None):
+    """uint8 repacked tensor-core operand (``mnb_repacked_bytes(K, N, bs)`` bytes)."""
+    torch = _torch()
+    lib = load_library()
+    _check_dev("packed", packed, torch.uint8)
+    if out is None:
+        nbytes = mnb_repacked_bytes(K, N, block_size)
+        if nbytes == 0:
+            raise MnbError(MNB_ERR_INVALID_ARG, "mnb_repack: invalid shape")
+        out = torch.empty(nbytes, dtype=torch.uint8, device=packed.device)
+    _check_dev("out", out, torch.uint8)
+    _raise(lib.mnb_repack(_ptr(packed), K, N, block_size, _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def mnb_gemv(A, packed, scales, zero_points, K: int, N: int, block_size: int, out=None, stream=None):
+    """fp16 ``[N]`` = A (fp16 ``[K]``) times the dequantised weight."""
+    torch = _torch()
+    lib = load_library()
+    _check_dev("A", A, torch.float16)
+    w = _weight(packed, scales, zero_points)
+    if out is None:
+        out = torch.empty(N, dtype=torch.float16, device=A.device)
+    _check_dev("out", out, torch.float16)
+    _raise(lib.mnb_gemv(_ptr(A), w, K, N, block_size, _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def mnb_gemm(A, packed, scales, zero_points, K: int, N: int, block_size: int, repacked=None,
+             workspace=None, out=None, stream=None):
+    """fp16 ``[M, N]`` = A (fp16 ``[M, K]``) times the dequantised weight."""
+    torch = _torch()
+    lib = load_library()
+    _check_dev("A", A, torch.float16)
+    M = A.numel() // K
+    w = _weight(packed, scales, zero_points)
+    _check_dev("repacked", repacked, torch.uint8)
+    need = mnb_workspace_bytes(M, K, N, block_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check_dev("out", out, torch.float16)
+    _raise(lib.mnb_gemm(_ptr(A), M, w, _ptr(repacked), K, N, block_size, _ptr(workspace), ws_bytes,
+                        _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def mnb_gemv_gate_up_swiglu(A, gate, up, K: int, N: int, block_size: int, out=None, stream=None):
+    """fp16 ``[N]`` = silu(A . gate^T) * (A . up^T); gate/up are (packed, scales, zero_points)."""
+    torch = _torch()
+    lib = load_library()
+    _check_dev("A", A, torch.float16)
+    wg = _weight(*gate)
+    wu = _weight(*up)
+    if out is None:
+        out = torch.empty(N, dtype=torch.float16, device=A.device)
+    _check_dev("out", out, torch.float16)
+    _raise(lib.mnb_gemv_gate_up_swiglu(_ptr(A), wg, wu, K, N, block_size, _ptr(out),
+                                       _stream_handle(stream)))
+    return out

@@ -1,0 +1,136 @@
+// Device helpers shared by the mnb kernels (CUDA side only).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace mnb {
+
+constexpr uint32_t kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------------------------
+// Programmatic dependent launch.  `pdl_wait` blocks until every kernel this one
+// depends on has finished and its writes are visible; before it a kernel may only
+// read buffers that no earlier kernel writes (the weights).  Both are no-ops when
+// the kernel was launched without programmatic stream serialisation.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 128-bit read-only streaming load that does not allocate in L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u16(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_nc_u8(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------------------------------------
+// Nibbles to exact fp16 (code - zp).
+//
+// A half whose bit pattern is 0x6400 | x (x < 1024) has the value 1024 + x, so OR-ing a
+// nibble into the low mantissa bits of 0x6400 gives 1024 + c, and a nibble sitting four
+// bits higher gives 1024 + 16 c.  Subtracting 1024 + zp, or scaling by 1/16 and
+// subtracting 64 + zp, leaves c - zp exactly (all values are small integers).  This is
+// the bit trick the fp16 GEMV of matmul_nbits.rs builds on; written here with the zero
+// point folded into the correction constants.
+//
+// For a 32-bit word with nibbles n0..n7 (bits 4p..4p+3 hold n_p) the results are the
+// half2 pairs (n0,n4), (n1,n5), (n2,n6), (n3,n7), low half first.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(orv));  // (a & b) | c
+  return r;
+}
+
+// Correction constants for zero point z (0..15): -(1024 + z) and -(64 + z), as half2.
+__device__ __forceinline__ uint32_t zp_lo_const(uint32_t z) { return (0xE400u + z) * 0x10001u; }
+__device__ __forceinline__ uint32_t zp_hi_const(uint32_t z) { return (0xD400u + 16u * z) * 0x10001u; }
+
+__device__ __forceinline__ void nibbles_to_centered_half2(uint32_t w, uint32_t zlo, uint32_t zhi,
+                                                          uint32_t d[4]) {
+  const uint32_t kMaskLo = 0x000f000fu, kMaskHi = 0x00f000f0u, kMagic = 0x64006400u;
+  const uint32_t kSixteenth = 0x2C002C00u;  // half2(1/16, 1/16)
+  const uint32_t t = w >> 8;
+  uint32_t h0 = lop3_and_or(w, kMaskLo, kMagic);
+  uint32_t h1 = lop3_and_or(w, kMaskHi, kMagic);
+  uint32_t h2 = lop3_and_or(t, kMaskLo, kMagic);
+  uint32_t h3 = lop3_and_or(t, kMaskHi, kMagic);
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d[0]) : "r"(h0), "r"(zlo));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d[1]) : "r"(h1), "r"(kSixteenth), "r"(zhi));
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d[2]) : "r"(h2), "r"(zlo));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d[3]) : "r"(h3), "r"(kSixteenth), "r"(zhi));
+}
+
+// Rearranges 8 consecutive halves (x = (a0,a1),(a2,a3),(a4,a5),(a6,a7)) into the pairs
+// (a0,a4), (a1,a5), (a2,a6), (a3,a7) that line up with nibbles_to_centered_half2.
+__device__ __forceinline__ void pair_halves_stride4(const uint4 x, uint32_t p[4]) {
+  p[0] = __byte_perm(x.x, x.z, 0x5410);
+  p[1] = __byte_perm(x.x, x.z, 0x7632);
+  p[2] = __byte_perm(x.y, x.w, 0x5410);
+  p[3] = __byte_perm(x.y, x.w, 0x7632);
+}
+
+// acc += w.lo * a.lo + w.hi * a.hi with exact fp16 x fp16 products and fp32 sums.
+__device__ __forceinline__ float fma2_f16_f32(uint32_t w, uint32_t a, float acc) {
+  asm("{\n\t.reg .b16 wl, wh, al, ah;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {al, ah}, %2;\n\t"
+      "fma.rn.f32.f16 %0, wl, al, %0;\n\t"
+      "fma.rn.f32.f16 %0, wh, ah, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w), "r"(a));
+  return acc;
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t h) {
+  return __half2float(__ushort_as_half((unsigned short)h));
+}
+
+// Sum of V per-lane values across a warp, V a power of two <= 32.  Each exchange step
+// halves the number of live values per lane, so V values cost V - 1 + (5 - log2 V)
+// shuffles.  Afterwards lane L holds the total of value (L >> (5 - log2 V)).
+template <int V>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[V], int lane) {
+  static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V must be a power of two");
+  int offset = 16;
+#pragma unroll
+  for (int cnt = V; cnt > 1; cnt >>= 1) {
+    const bool upper = (lane & offset) != 0;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; ++i) {
+      const float keep = upper ? v[i + cnt / 2] : v[i];
+      const float send = upper ? v[i] : v[i + cnt / 2];
+      v[i] = keep + __shfl_xor_sync(kFull, send, offset);
+    }
+    offset >>= 1;
+  }
+  float r = v[0];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (o <= offset) r += __shfl_xor_sync(kFull, r, o);
+  }
+  return r;
+}
+
+}  // namespace mnb

@@ -1,0 +1,57 @@
+// Host-side declarations shared by the mnb translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mnb {
+
+struct QWeight {
+  const uint8_t* packed;
+  const void* scales;
+  const uint8_t* zp;
+  int scales_f16;  // 1: fp16 scales, 0: fp32
+};
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  bool pdl;         // launch with programmatic stream serialisation
+  int num_sms;
+  const char* variant = nullptr;  // set by the launcher that ran
+};
+
+// Each launcher returns cudaSuccess or the launch error.  Shapes are validated by the
+// caller (api.cu).
+cudaError_t launch_dequant(LaunchCtx& ctx, const QWeight& w, int K, int N, int bs, float* out);
+cudaError_t launch_repack(LaunchCtx& ctx, const uint8_t* packed, int K, int N, uint8_t* out);
+// Fast M = 1 GEMV; returns cudaErrorNotSupported when the shape has no fast variant.
+cudaError_t launch_gemv(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs,
+                        void* Y);
+cudaError_t launch_gemv_pair_swiglu(LaunchCtx& ctx, const void* A, const QWeight& gate,
+                                    const QWeight& up, int K, int N, int bs, void* out);
+// Any M, any K % 16 == 0: CUDA-core kernel, fp32 arithmetic.
+cudaError_t launch_generic(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N,
+                           int bs, void* Y);
+cudaError_t launch_generic_pair_swiglu(LaunchCtx& ctx, const void* A, const QWeight& gate,
+                                       const QWeight& up, int K, int N, int bs, void* out);
+
+// Launch helper: cudaLaunchKernelEx with the programmatic-serialisation attribute when
+// ctx.pdl is set.
+template <typename Kern, typename... Args>
+cudaError_t launch_kernel(LaunchCtx& ctx, Kern kernel, dim3 grid, dim3 block, size_t smem,
+                          Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = ctx.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace mnb

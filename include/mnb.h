@@ -1,0 +1,171 @@
+/*
+ * mnb.h -- block-quantized INT4 (MatMulNBits) products on one GB300 GPU (sm_103a).
+ *
+ * The library computes Y[M,N] = A[M,K] . dequant(B)^T for weights stored in the
+ * ONNX com.microsoft::MatMulNBits layout, as spelled out in
+ *   onnx-runtime-ep-cuda 0.1.0-dev.6, src/kernels/marlin_gemm.rs, module doc,
+ *   section "ONNX MatMulNBits int4 format", and
+ *   onnx-runtime-ep-cuda 0.1.0-dev.3, src/kernels/matmul_nbits.rs, kernel
+ *   matmul_nbits_dequant_f32:
+ *
+ *   packed       uint8 [N, k_blocks, bs/2], k_blocks = K/bs. The nibble for (n, k) is in
+ *                byte (n*k_blocks + k/bs)*(bs/2) + (k%bs)/2: low nibble for even k,
+ *                high nibble for odd k. code in 0..15. (With K % bs == 0 every row is
+ *                simply K/2 consecutive bytes.)
+ *   scales       [N, k_blocks], fp16 or fp32.
+ *   zero_points  optional uint8 [N, ceil(k_blocks/2)]: the nibble for (n, g) is in byte
+ *                n*ceil(k_blocks/2) + g/2, low nibble for even g. NULL means zp = 8.
+ *   dequant(B)[n, k] = (code[n, k] - zp[n, k/bs]) * scale[n, k/bs].
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is device memory owned by the caller; the library keeps
+ *     no reference after the call returns and allocates nothing.
+ *   - A and Y are fp16 (IEEE binary16, passed as raw 16-bit storage), row-major.
+ *   - Every device pointer must be non-NULL (except zero_points, workspace when
+ *     ws_bytes is 0, and repacked where stated) and 16-byte aligned:
+ *     otherwise MNB_ERR_INVALID_ARG / MNB_ERR_MISALIGNED.
+ *   - block_size must be 16, 32, 64 or 128 and K a multiple of it; K, N, M >= 1 and
+ *     K, N <= 2^24, M <= 2^20. Otherwise MNB_ERR_INVALID_ARG or MNB_ERR_UNSUPPORTED.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream)
+ *     and runs asynchronously: the call neither synchronises nor copies to the host,
+ *     so every compute call may be captured into a CUDA graph. Launch geometry depends
+ *     only on the shape arguments and the device.
+ *   - Errors never throw. A non-MNB_OK status leaves a message for mnb_last_error()
+ *     (per host thread). MNB_ERR_CUDA carries the CUDA error string.
+ *   - Results are deterministic: the same inputs give the same bits on every run.
+ */
+#ifndef MNB_H_
+#define MNB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MNB_API __attribute__((visibility("default")))
+#else
+#define MNB_API
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+typedef struct CUstream_st *mnb_stream;
+
+typedef enum {
+    MNB_OK = 0,
+    MNB_ERR_INVALID_ARG = 1,  /* bad shape, block size, NULL pointer, or dtype */
+    MNB_ERR_UNSUPPORTED = 2,  /* valid for the format, but not handled by this build */
+    MNB_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
+    MNB_ERR_CAPTURE = 4,      /* the call is refused while `stream` is being captured */
+    MNB_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+    MNB_ERR_TIMEOUT = 6       /* a bounded device-side wait gave up (kernel status word) */
+} mnb_status;
+
+typedef enum { MNB_F16 = 0, MNB_F32 = 1 } mnb_dtype;
+
+/* One quantised weight: the MatMulNBits tuple (packed, scales, zero_points). */
+typedef struct {
+    const uint8_t *packed;      /* [N, K/2] bytes                                   */
+    const void *scales;         /* [N, K/bs] of fp16 or fp32 (scales_dtype)          */
+    int32_t scales_dtype;       /* MNB_F16 or MNB_F32                                */
+    const uint8_t *zero_points; /* [N, ceil(K/bs/2)] nibbles, or NULL for zp = 8      */
+} mnb_weight;
+
+/*
+ * Dequantise to fp32 [K, N] (row k, column n at out_kn[k*N + n]).
+ * Follows matmul_nbits_dequant_f32 (matmul_nbits.rs): element (code - zp) * scale.
+ * The product is rounded once to fp32 (round to nearest even); it is exact for fp16
+ * scales. out_kn holds K*N floats.
+ */
+MNB_API mnb_status mnb_dequant(mnb_weight w, int K, int N, int block_size, float *out_kn,
+                       mnb_stream stream);
+
+/*
+ * Size in bytes of the repacked tensor-core operand for a K x N weight:
+ * ceil(N/128)*128 * ceil(K/64)*64 / 2. Returns 0 for invalid arguments.
+ */
+MNB_API size_t mnb_repacked_bytes(int K, int N, int block_size);
+
+/*
+ * Reorder `packed` into this library's tensor-core operand layout (a bijection on the
+ * codes; scales and zero points keep their MatMulNBits indexing). The pages repack
+ * once for their mma.sync kernel (marlin_gemm.rs, "Repacked weight layout"); the layout
+ * here is new, built for 1-D bulk copies and shared-memory dequantisation:
+ *   tile t (128 rows) and k-block b (64 k) form one 4096-byte block at
+ *   (t * ceil(K/64) + b) * 4096; in it the 16 bytes at q*2048 + r*16 (q in 0..1,
+ *   r in 0..127) hold the codes of row n = 128t + r for k = 64b + 32q + i, i in 0..31,
+ *   as four little-endian 32-bit words; word j = i/8 keeps i at nibble p (bits 4p..4p+3)
+ *   where i = 8j + 2(p%4) + p/4. Codes outside the K x N weight are 0.
+ * `out` holds mnb_repacked_bytes(K, N, block_size) bytes. Runs once per weight, so it is
+ * refused with MNB_ERR_CAPTURE while `stream` is capturing (a repack inside a graph
+ * would be replayed on every launch).
+ */
+MNB_API mnb_status mnb_repack(const uint8_t *packed, int K, int N, int block_size, uint8_t *out,
+                      mnb_stream stream);
+
+/*
+ * Decode GEMV, M = 1: Y[n] = sum_k A[k] * dequant(B)[n, k], stored as fp16 (round to
+ * nearest even from the fp32 accumulator). A is fp16 [K], Y is fp16 [N].
+ * The per-group partial dot of (code - zp) and A is scaled after it is formed
+ * (matmul_nbits.rs, matmul_nbits_gemv_f16; marlin_gemm.rs, "Per-group scale applied
+ * after the tensor-core accumulate"). |Y - exact| <= 2e-3 * sum_k |a_k w_nk| + 1e-5.
+ */
+MNB_API mnb_status mnb_gemv(const void *A, mnb_weight w, int K, int N, int block_size, void *Y,
+                    mnb_stream stream);
+
+/*
+ * Scratch bytes mnb_gemm needs for this shape (0 when none). The caller allocates it
+ * once and passes it to every call of that shape; its contents need no initialisation.
+ */
+MNB_API size_t mnb_workspace_bytes(int M, int K, int N, int block_size);
+
+/*
+ * Y[M, N] = A[M, K] . dequant(B)^T, fp16 in and out, fp32 accumulation.
+ * M = 1 runs the GEMV. 2 <= M <= 16 (speculative verify) streams the MatMulNBits
+ * storage directly; `repacked` may be NULL and is not read. M > 16 needs the repacked
+ * operand from mnb_repack (`repacked` NULL gives MNB_ERR_INVALID_ARG) and runs on the
+ * tcgen05 tensor cores,
+ * the group scale applied to each group's partial accumulator (marlin_gemm.rs,
+ * matmul_nbits_marlin_gemm_f16). `workspace`/`ws_bytes`: see mnb_workspace_bytes;
+ * a smaller workspace gives MNB_ERR_INVALID_ARG.
+ */
+MNB_API mnb_status mnb_gemm(const void *A, int M, mnb_weight w, const uint8_t *repacked, int K, int N,
+                    int block_size, void *workspace, size_t ws_bytes, void *Y,
+                    mnb_stream stream);
+
+/*
+ * Paired gate/up projection with the SwiGLU epilogue (matmul_nbits.rs,
+ * matmul_nbits_gemv_f16_gate_up_swiglu): g = A . gate^T, u = A . up^T (both M = 1,
+ * same K, N, block_size), out[n] = silu(g[n]) * u[n] with silu(x) = x / (1 + e^-x),
+ * computed in fp32 from the fp32 accumulators and stored as fp16. A is fp16 [K],
+ * out is fp16 [N]. Each weight may use its own scale dtype and zero points.
+ */
+MNB_API mnb_status mnb_gemv_gate_up_swiglu(const void *A, mnb_weight gate, mnb_weight up, int K, int N,
+                                   int block_size, void *out, mnb_stream stream);
+
+/*
+ * Programmatic dependent launch. With `enable` != 0, later calls on this host thread
+ * launch their kernels with programmatic stream serialisation: a kernel may start while
+ * the previous kernel on the stream is still running, and it streams its weight, scale
+ * and zero-point buffers before waiting for that kernel to finish; it reads A and writes
+ * Y only after the wait. Enable it only when no earlier work on the stream writes the
+ * weight buffers (weights that stay constant during inference). Default: off.
+ */
+MNB_API void mnb_set_programmatic_launch(int enable);
+
+/* Message of the last failed call on this host thread ("" if none). */
+MNB_API const char *mnb_last_error(void);
+
+/* Name of the kernel variant the last successful call on this host thread launched. */
+MNB_API const char *mnb_last_variant(void);
+
+/* Library version string. */
+MNB_API const char *mnb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MNB_H_ */

@@ -1,0 +1,329 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bit-exact for the dequantised weights and the repacked operand; within
+|y - y_ref| <= 2e-3 * sum_k |a_k w_nk| + 1e-5 per element for every product.  Shapes
+cover the measured workloads at full size, ragged tails (N not a multiple of the
+column tile, M not a multiple of the row tile), every block size, both scale dtypes,
+with and without zero points, and each kernel variant the dispatcher can pick.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import mnb_synth as syn
+from oracle import mnb_oracle as orc
+from tests.helpers import assert_within_bound, upload_act, upload_weight
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import gemm_mnb_gemv_gb300 as mnb
+    return mnb, torch, torch.device("cuda:0")
+
+
+DEQUANT_CASES = [
+    ("dq_tiny", 256, 128, 32, "f16", True),
+    ("dq_ragged16", 96, 130, 16, "f32", True),
+    ("dq_ragged64", 192, 200, 64, "f16", False),
+    ("dq_f32_128", 512, 77, 128, "f32", True),
+    ("dq_attnproj", 4096, 4096, 32, "f16", True),
+]
+
+
+@pytest.mark.parametrize("name,K,N,bs,sdt,zp", DEQUANT_CASES)
+def test_dequant_bit_exact(env, name, K, N, bs, sdt, zp):
+    mnb, torch, dev = env
+    wl = syn.custom(name, 1, K, N, bs, scales_dtype=sdt, has_zp=zp)
+    w = syn.make_weight(wl)
+    out = mnb.mnb_dequant(*upload_weight(w, dev), K, N, bs)
+    torch.cuda.synchronize()
+    ref = orc.dequant_kn_f32(w.packed, w.scales, w.zero_points, K, N, bs)
+    got = out.cpu().numpy()
+    assert got.shape == (K, N)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_prefill_weight_bit_exact(env):
+    mnb, torch, dev = env
+    wl = syn.WORKLOADS["prefill_m2048_k4096_n14336"]
+    w = syn.make_weight(wl)
+    out = mnb.mnb_dequant(*upload_weight(w, dev), wl.K, wl.N, wl.block_size)
+    ref = orc.dequant_kn_f32(w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("K,N,bs", [(64, 1, 16), (96, 130, 32), (256, 128, 64), (192, 257, 128),
+                                    (4096, 14336, 128)])
+def test_repack_bit_exact(env, K, N, bs):
+    mnb, torch, dev = env
+    packed = syn.random_bytes(syn.fnv1a64(f"repack/{K}/{N}"), N * K // 2).reshape(N, K // 2)
+    out = mnb.mnb_repack(torch.from_numpy(packed).to(dev), K, N, bs)
+    ref = orc.repack(packed, K, N, bs)
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+GEMV_CASES = [
+    # name, K, N, bs, scales, zp, act  -- chosen to hit every fast-GEMV geometry
+    ("gv_one_col", 64, 1, 16, "f16", True, "normal"),
+    ("gv_ragged32", 96, 130, 32, "f16", True, "normal"),
+    ("gv_ragged64", 192, 200, 64, "f32", False, "normal"),
+    ("gv_bs128", 384, 333, 128, "f32", True, "normal"),
+    ("gv_bs16_mid", 2048, 301, 16, "f16", True, "normal"),
+    ("gv_k8192", 8192, 300, 64, "f16", True, "normal"),
+    ("gv_k16384", 16384, 100, 32, "f32", True, "normal"),
+    ("gv_k32768", 32768, 70, 128, "f16", False, "normal"),
+    ("gv_generic_k48", 48, 5, 16, "f16", True, "normal"),
+    ("gv_generic_k65536", 65536, 9, 64, "f16", True, "normal"),
+]
+
+
+@pytest.mark.parametrize("name,K,N,bs,sdt,zp,act", GEMV_CASES)
+def test_gemv_parity(env, name, K, N, bs, sdt, zp, act):
+    mnb, torch, dev = env
+    wl = syn.custom(name, 1, K, N, bs, scales_dtype=sdt, has_zp=zp, act=act)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    y = mnb.mnb_gemv(upload_act(A.reshape(-1), dev), *upload_weight(w, dev), K, N, bs)
+    variant = mnb.mnb_last_variant()
+    torch.cuda.synchronize()
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
+    assert_within_bound(y.cpu().numpy()[None, :], Y, B, name)
+    expect_generic = (K % 32 != 0) or K > 32768
+    assert variant.startswith("generic") == expect_generic, variant
+
+
+@pytest.mark.parametrize("wname", ["tiny_gemv_k256_n128", "gemv_attnproj_k4096_n4096",
+                                   "mlp_down_k14336_n4096"])
+def test_gemv_workloads_full_size(env, wname):
+    mnb, torch, dev = env
+    wl = syn.WORKLOADS[wname]
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    y = mnb.mnb_gemv(upload_act(A.reshape(-1), dev), *upload_weight(w, dev), wl.K, wl.N, wl.block_size)
+    torch.cuda.synchronize()
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size)
+    assert_within_bound(y.cpu().numpy()[None, :], Y, B, wname)
+
+
+def _swiglu_case(env, wl):
+    mnb, torch, dev = env
+    wg = syn.make_weight(wl, "gate")
+    wu = syn.make_weight(wl, "up")
+    A = syn.make_activation(wl)
+    out = mnb.mnb_gemv_gate_up_swiglu(upload_act(A.reshape(-1), dev), upload_weight(wg, dev),
+                                      upload_weight(wu, dev), wl.K, wl.N, wl.block_size)
+    torch.cuda.synchronize()
+    ref, g, bg, u, bu = orc.gate_up_swiglu(A, (wg.packed, wg.scales, wg.zero_points),
+                                           (wu.packed, wu.scales, wu.zero_points),
+                                           wl.K, wl.N, wl.block_size)
+    tol = orc.swiglu_tolerance(g, bg, u, bu, ref)
+    got = out.cpu().numpy().astype(np.float64)[None, :]
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref)
+    assert np.all(err <= tol), f"worst excess {float(np.max(err - tol)):.3e}"
+
+
+def test_gate_up_swiglu_workload_full_size(env):
+    _swiglu_case(env, syn.WORKLOADS["mlp_gate_up_k4096_n14336"])
+
+
+@pytest.mark.parametrize("K,N,bs,sdt,zp", [(256, 130, 32, "f16", True), (1024, 77, 16, "f32", False),
+                                           (8192, 65, 64, "f16", True), (48, 9, 16, "f16", True)])
+def test_gate_up_swiglu_ragged(env, K, N, bs, sdt, zp):
+    _swiglu_case(env, syn.custom(f"sw_{K}_{N}_{bs}", 1, K, N, bs, scales_dtype=sdt, has_zp=zp))
+
+
+@pytest.mark.parametrize("M", [2, 4, 8, 16])
+def test_gemm_small_m_workloads_full_size(env, M):
+    mnb, torch, dev = env
+    wl = syn.WORKLOADS[f"verify_m{M}_k4096_n4096"]
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    y = mnb.mnb_gemm(upload_act(A, dev), *upload_weight(w, dev), wl.K, wl.N, wl.block_size)
+    torch.cuda.synchronize()
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size)
+    assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
+
+
+@pytest.mark.parametrize("M,K,N,bs", [(3, 96, 130, 32), (5, 192, 200, 64), (13, 384, 77, 128),
+                                      (7, 48, 33, 16), (16, 1024, 129, 16)])
+def test_gemm_small_m_ragged(env, M, K, N, bs):
+    mnb, torch, dev = env
+    wl = syn.custom(f"sm_{M}_{K}_{N}_{bs}", M, K, N, bs)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    y = mnb.mnb_gemm(upload_act(A, dev), *upload_weight(w, dev), K, N, bs)
+    torch.cuda.synchronize()
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
+    assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
+
+
+@pytest.mark.parametrize("M,K,N,bs,sdt,zp", [(17, 128, 130, 32, "f16", True),
+                                             (64, 256, 256, 128, "f16", True),
+                                             (200, 320, 384, 64, "f32", False),
+                                             (300, 1024, 520, 16, "f16", True),
+                                             (256, 4096, 512, 128, "f16", True)])
+def test_gemm_large_m_ragged(env, M, K, N, bs, sdt, zp):
+    mnb, torch, dev = env
+    wl = syn.custom(f"lm_{M}_{K}_{N}_{bs}", M, K, N, bs, scales_dtype=sdt, has_zp=zp)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    packed, scales, zpt = upload_weight(w, dev)
+    rp = mnb.mnb_repack(packed, K, N, bs)
+    y = mnb.mnb_gemm(upload_act(A, dev), packed, scales, zpt, K, N, bs, repacked=rp)
+    torch.cuda.synchronize()
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
+    assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
+
+
+def test_gemm_prefill_full_size_sampled_rows(env):
+    """Full-size prefill (M=2048, K=4096, N=14336, bs=128): 24 whole output rows checked,
+    spread over every 128-row tile, plus all outputs finite."""
+    mnb, torch, dev = env
+    wl = syn.WORKLOADS["prefill_m2048_k4096_n14336"]
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    packed, scales, zpt = upload_weight(w, dev)
+    rp = mnb.mnb_repack(packed, wl.K, wl.N, wl.block_size)
+    y = mnb.mnb_gemm(upload_act(A, dev), packed, scales, zpt, wl.K, wl.N, wl.block_size, repacked=rp)
+    torch.cuda.synchronize()
+    yc = y.cpu().numpy()
+    assert np.all(np.isfinite(yc.astype(np.float32)))
+    rows = np.array(sorted(set([0, 1, 127, 128, 255, 1023, 1024, 2046, 2047] +
+                               [int(r) for r in np.random.default_rng(3).integers(0, 2048, 15)])))
+    a = orc.activations_f64(A[rows])
+    W = orc.weight_nk(w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size)
+    Y = a @ W.T
+    B = np.abs(a) @ np.abs(W).T
+    assert_within_bound(yc[rows], Y, B, "prefill rows")
+
+
+def test_all_codes_equal_zero_point_gives_exact_zero(env):
+    mnb, torch, dev = env
+    K, N, bs = 512, 96, 32
+    G = K // bs
+    rng = np.random.default_rng(11)
+    zp_ng = rng.integers(0, 16, size=(N, G))
+    codes = np.repeat(zp_ng, bs, axis=1).astype(np.uint8)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    zp = np.zeros((N, G // 2), dtype=np.uint8)
+    zp |= zp_ng[:, 0::2].astype(np.uint8)
+    zp |= (zp_ng[:, 1::2].astype(np.uint8) << 4)
+    scales = rng.uniform(0.01, 2, size=(N, G)).astype(np.float16)
+    A = rng.standard_normal((4, K)).astype(np.float16)
+    t = lambda x: torch.from_numpy(x).to(dev)
+    y1 = mnb.mnb_gemv(t(A[0]), t(packed), t(scales), t(zp), K, N, bs)
+    y4 = mnb.mnb_gemm(t(A), t(packed), t(scales), t(zp), K, N, bs)
+    torch.cuda.synchronize()
+    assert np.all(y1.cpu().numpy() == 0) and np.all(y4.cpu().numpy() == 0)
+
+
+def test_adversarial_extremes(env):
+    """|a| = 4 everywhere and codes at 0/15 against zero points 15/0: the largest terms."""
+    mnb, torch, dev = env
+    K, N, bs = 4096, 64, 32
+    G = K // bs
+    rng = np.random.default_rng(12)
+    codes = np.where(rng.random((N, K)) < 0.5, 0, 15).astype(np.uint8)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    zp_ng = np.where(rng.random((N, G)) < 0.5, 0, 15).astype(np.uint8)
+    zp = (zp_ng[:, 0::2] | (zp_ng[:, 1::2] << 4)).astype(np.uint8)
+    scales = np.full((N, G), 0.02, dtype=np.float16)
+    A = np.where(rng.random((1, K)) < 0.5, -4.0, 4.0).astype(np.float16)
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    y = mnb.mnb_gemv(t(A[0]), t(packed), t(scales), t(zp), K, N, bs)
+    torch.cuda.synchronize()
+    Y, B = orc.matmul(A, packed, scales, zp, K, N, bs)
+    assert_within_bound(y.cpu().numpy()[None, :], Y, B, "extremes")
+
+
+def test_results_are_deterministic(env):
+    mnb, torch, dev = env
+    wl = syn.WORKLOADS["verify_m8_k4096_n4096"]
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    wt = upload_weight(w, dev)
+    a = upload_act(A, dev)
+    r1 = mnb.mnb_gemm(a, *wt, wl.K, wl.N, wl.block_size).clone()
+    r2 = mnb.mnb_gemm(a, *wt, wl.K, wl.N, wl.block_size).clone()
+    g1 = mnb.mnb_gemv(a[0].contiguous(), *wt, wl.K, wl.N, wl.block_size).clone()
+    g2 = mnb.mnb_gemv(a[0].contiguous(), *wt, wl.K, wl.N, wl.block_size).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(r1, r2) and torch.equal(g1, g2)
+
+
+def test_graph_capture_replay_matches_eager(env):
+    mnb, torch, dev = env
+    wl = syn.WORKLOADS["gemv_attnproj_k4096_n4096"]
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl, rows=4)
+    wt = upload_weight(w, dev)
+    a = upload_act(A, dev)
+    y1 = torch.empty(wl.N, dtype=torch.float16, device=dev)
+    y4 = torch.empty((4, wl.N), dtype=torch.float16, device=dev)
+    e1 = mnb.mnb_gemv(a[0].contiguous(), *wt, wl.K, wl.N, wl.block_size).clone()
+    e4 = mnb.mnb_gemm(a, *wt, wl.K, wl.N, wl.block_size).clone()
+    a0 = a[0].contiguous()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            mnb.mnb_gemv(a0, *wt, wl.K, wl.N, wl.block_size, out=y1)
+            mnb.mnb_gemm(a, *wt, wl.K, wl.N, wl.block_size, out=y4)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y1, e1) and torch.equal(y4, e4)
+
+
+def test_repack_is_refused_during_capture(env):
+    mnb, torch, dev = env
+    K, N, bs = 256, 128, 32
+    packed = torch.zeros((N, K // 2), dtype=torch.uint8, device=dev)
+    out = torch.empty(mnb.mnb_repacked_bytes(K, N, bs), dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    status = None
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            try:
+                mnb.mnb_repack(packed, K, N, bs, out=out)
+            except mnb.MnbError as e:
+                status = e.status
+    assert status == mnb.MNB_ERR_CAPTURE
+
+
+def test_programmatic_launch_gives_same_bits(env):
+    """A chain of GEMVs where each reads the previous output, with and without
+    programmatic dependent launch: identical results."""
+    mnb, torch, dev = env
+    wl = syn.WORKLOADS["gemv_attnproj_k4096_n4096"]
+    ws = [upload_weight(syn.make_weight(wl, f"chain{i}"), dev) for i in range(4)]
+    a = upload_act(syn.make_activation(wl).reshape(-1), dev)
+
+    def run():
+        x = a
+        outs = []
+        for w in ws:
+            x = mnb.mnb_gemv(x, *w, wl.K, wl.N, wl.block_size)
+            outs.append(x)
+        torch.cuda.synchronize()
+        return [o.clone() for o in outs]
+
+    base = run()
+    mnb.mnb_set_programmatic_launch(True)
+    try:
+        pdl = run()
+    finally:
+        mnb.mnb_set_programmatic_launch(False)
+    for b, p in zip(base, pdl):
+        assert torch.equal(b, p)
