@@ -218,9 +218,11 @@ class DeviceBench:
 
         ms, g = self.time_graph(rec, calls, steps, warmup, sampler)
         us = ms * 1e3 / calls
+        # The graph holds raw pointers into `copies`, A and Y: keep them alive with it.
         return {"workload": wl.name, "us_per_call": us, "gbps": call_bytes(wl) / (us * 1e3),
                 "copies": ncopy, "calls_per_replay": calls, "ms_per_replay": ms,
-                "variant": mnb.mnb_last_variant(), "graph": g, "A": A, "Y": Y, "w": w}
+                "variant": mnb.mnb_last_variant(), "graph": g, "A": A, "Y": Y, "w": w,
+                "buffers": copies}
 
     def swiglu(self, wl, steps, warmup, sampler, calls=200):
         torch, mnb = self.torch, self.mnb
@@ -286,6 +288,11 @@ class DeviceBench:
                 "h2d_bytes_per_step": int(A_host.numel() * 2),
                 "d2h_bytes_per_step": int(Y_host.numel() * 2),
                 "note": "pinned host A -> device, one graph replay of the 1000 calls, device Y -> pinned host, synchronised, per step"}
+
+
+def log(msg: str):
+    if int(os.environ.get("RANK", "0")) == 0:
+        print(msg, file=sys.stderr, flush=True)
 
 
 # ---------------------------------------------------------------------------------
@@ -422,17 +429,22 @@ def main():
 
     wl = syn.WORKLOADS[HEADLINE]
     head = db.gemv(wl, args.steps, args.warmup, sampler)
+    log(f"headline {head['us_per_call']:.3f} us/call {head['gbps']:.1f} GB/s ({head['variant']})")
     launches_headline = args.steps * CALLS_PER_STEP
     extras = {}
     if not args.quick:
         extras["gate_up_swiglu"] = db.swiglu(syn.WORKLOADS["mlp_gate_up_k4096_n14336"], 20, 3, sampler)
         d = db.gemv(syn.WORKLOADS["mlp_down_k14336_n4096"], 20, 3, sampler, calls=200)
-        extras["down_gemv"] = {k: v for k, v in d.items() if k not in ("graph", "A", "Y", "w")}
+        extras["down_gemv"] = {k: v for k, v in d.items() if k not in ("graph", "A", "Y", "w", "buffers")}
+        del d
         for M in (2, 4, 8, 16):
             extras[f"verify_m{M}"] = db.gemm(syn.WORKLOADS[f"verify_m{M}_k4096_n4096"], 20, 3, sampler,
                                              calls=200, repacked=False)
         extras["prefill"] = db.gemm(syn.WORKLOADS["prefill_m2048_k4096_n14336"], 10, 3, sampler,
                                     calls=9, repacked=True)
+    for k, v in extras.items():
+        log(f"{k}: {v['us_per_call']:.3f} us/call, {v.get('gbps', 0):.1f} GB/s, "
+            f"{v.get('tflops', 0):.1f} TFLOP/s ({v['variant']})")
     clocks = sampler.stop()
     e2e = db.e2e_gemv(head, max(3, args.steps // 10))
 

@@ -8,7 +8,8 @@ output tensor is not passed, the binding allocates it with torch before the call
 
 The names match the C entry points: ``mnb_dequant``, ``mnb_repacked_bytes``,
 ``mnb_repack``, ``mnb_gemv``, ``mnb_workspace_bytes``, ``mnb_gemm``,
-``mnb_gemv_gate_up_swiglu``, ``mnb_set_programmatic_launch``, ``mnb_last_error``,
+``mnb_gemv_gate_up_swiglu``, ``mnb_set_programmatic_launch``, ``mnb_check_device_status``,
+``mnb_last_error``,
 ``mnb_last_variant``, ``mnb_version``.
 """
 from __future__ import annotations
@@ -60,6 +61,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mnb_gemm": (c_int, [vp, c_int, MnbWeight, vp, c_int, c_int, c_int, vp, c_size, vp, vp]),
         "mnb_gemv_gate_up_swiglu": (c_int, [vp, MnbWeight, MnbWeight, c_int, c_int, c_int, vp, vp]),
         "mnb_set_programmatic_launch": (None, [c_int]),
+        "mnb_check_device_status": (c_int, []),
         "mnb_last_error": (ctypes.c_char_p, []),
         "mnb_last_variant": (ctypes.c_char_p, []),
         "mnb_version": (ctypes.c_char_p, []),
@@ -133,6 +135,11 @@ def mnb_version() -> str:
 
 def mnb_set_programmatic_launch(enable: bool) -> None:
     load_library().mnb_set_programmatic_launch(1 if enable else 0)
+
+
+def mnb_check_device_status() -> None:
+    """Raises MnbError(MNB_ERR_TIMEOUT) if a device-side bounded wait gave up since the last check."""
+    _raise(load_library().mnb_check_device_status())
 
 
 def mnb_repacked_bytes(K: int, N: int, block_size: int) -> int:

@@ -7,6 +7,7 @@
 // message instead of an exception (the EpError::KernelFailed strings of matmul_nbits.rs).
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "../../include/mnb.h"
@@ -15,6 +16,21 @@
 namespace {
 
 thread_local std::string g_last_error;
+
+// Set (bitwise OR) by a kernel whose bounded device-side wait gave up.
+__device__ uint32_t g_device_status;
+std::mutex g_status_mu;
+uint32_t* g_status_ptr[128] = {};
+
+uint32_t* device_status_ptr(int dev) {
+  if (dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_status_ptr[dev];
+}
 thread_local const char* g_last_variant = "";
 thread_local bool g_pdl = false;
 
@@ -79,8 +95,19 @@ mnb_status make_ctx(const char* fn, mnb_stream stream, mnb::LaunchCtx* ctx) {
   ctx->stream = reinterpret_cast<cudaStream_t>(stream);
   ctx->pdl = g_pdl;
   ctx->num_sms = sms;
+  ctx->status = device_status_ptr(dev);
   ctx->variant = nullptr;
   return MNB_OK;
+}
+
+// M = 1: the bulk-copy ring kernel when rows are 16-byte multiples, else the
+// register-pipelined kernel, else the generic kernel.
+cudaError_t run_gemv(mnb::LaunchCtx& ctx, const void* A, const mnb::QWeight& q, int K, int N, int bs,
+                     void* Y) {
+  cudaError_t e = mnb::launch_gemv_tma(ctx, A, q, K, N, bs, Y);
+  if (e == cudaErrorNotSupported) e = mnb::launch_gemv(ctx, A, q, K, N, bs, Y);
+  if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, 1, q, K, N, bs, Y);
+  return e;
 }
 
 mnb_status finish(const char* fn, cudaError_t e, const mnb::LaunchCtx& ctx) {
@@ -99,6 +126,24 @@ const char* mnb_last_error(void) { return g_last_error.c_str(); }
 const char* mnb_last_variant(void) { return g_last_variant; }
 const char* mnb_version(void) { return "mnb 0.1.0 (sm_103a)"; }
 void mnb_set_programmatic_launch(int enable) { g_pdl = enable != 0; }
+
+mnb_status mnb_check_device_status(void) {
+  const char* fn = "mnb_check_device_status";
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  uint32_t v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  if (v == 0) {
+    g_last_error.clear();
+    return MNB_OK;
+  }
+  const uint32_t zero = 0;
+  e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  return fail(MNB_ERR_TIMEOUT, "%s: a device-side wait gave up (status bits 0x%x: 1 = stage wait, "
+              "2 = slot wait, 4 = tensor-core pipeline wait); outputs of that call are NaN", fn, v);
+}
 
 mnb_status mnb_dequant(mnb_weight w, int K, int N, int block_size, float* out_kn,
                        mnb_stream stream) {
@@ -150,9 +195,7 @@ mnb_status mnb_gemv(const void* A, mnb_weight w, int K, int N, int block_size, v
   if ((st = check_ptr(fn, "Y", Y)) != MNB_OK) return st;
   mnb::LaunchCtx ctx;
   if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
-  cudaError_t e = mnb::launch_gemv(ctx, A, q, K, N, block_size, Y);
-  if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, 1, q, K, N, block_size, Y);
-  return finish(fn, e, ctx);
+  return finish(fn, run_gemv(ctx, A, q, K, N, block_size, Y), ctx);
 }
 
 size_t mnb_workspace_bytes(int M, int K, int N, int block_size) {
@@ -185,8 +228,7 @@ mnb_status mnb_gemm(const void* A, int M, mnb_weight w, const uint8_t* repacked,
   if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
   cudaError_t e;
   if (M == 1) {
-    e = mnb::launch_gemv(ctx, A, q, K, N, block_size, Y);
-    if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, 1, q, K, N, block_size, Y);
+    e = run_gemv(ctx, A, q, K, N, block_size, Y);
   } else {
     e = mnb::launch_generic(ctx, A, M, q, K, N, block_size, Y);
   }
@@ -205,7 +247,8 @@ mnb_status mnb_gemv_gate_up_swiglu(const void* A, mnb_weight gate, mnb_weight up
   if ((st = check_ptr(fn, "out", out)) != MNB_OK) return st;
   mnb::LaunchCtx ctx;
   if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
-  cudaError_t e = mnb::launch_gemv_pair_swiglu(ctx, A, g, u, K, N, block_size, out);
+  cudaError_t e = mnb::launch_gemv_pair_swiglu_tma(ctx, A, g, u, K, N, block_size, out);
+  if (e == cudaErrorNotSupported) e = mnb::launch_gemv_pair_swiglu(ctx, A, g, u, K, N, block_size, out);
   if (e == cudaErrorNotSupported) e = mnb::launch_generic_pair_swiglu(ctx, A, g, u, K, N, block_size, out);
   return finish(fn, e, ctx);
 }

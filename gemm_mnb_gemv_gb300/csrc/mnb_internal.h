@@ -18,6 +18,7 @@ struct LaunchCtx {
   cudaStream_t stream;
   bool pdl;         // launch with programmatic stream serialisation
   int num_sms;
+  uint32_t* status = nullptr;     // device status word for bounded waits
   const char* variant = nullptr;  // set by the launcher that ran
 };
 
@@ -25,7 +26,12 @@ struct LaunchCtx {
 // caller (api.cu).
 cudaError_t launch_dequant(LaunchCtx& ctx, const QWeight& w, int K, int N, int bs, float* out);
 cudaError_t launch_repack(LaunchCtx& ctx, const uint8_t* packed, int K, int N, uint8_t* out);
-// Fast M = 1 GEMV; returns cudaErrorNotSupported when the shape has no fast variant.
+// Bulk-copy ring GEMV (M = 1); cudaErrorNotSupported when rows are not 16-byte multiples.
+cudaError_t launch_gemv_tma(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs,
+                            void* Y);
+cudaError_t launch_gemv_pair_swiglu_tma(LaunchCtx& ctx, const void* A, const QWeight& gate,
+                                        const QWeight& up, int K, int N, int bs, void* out);
+// Register-pipelined M = 1 GEMV; cudaErrorNotSupported when the shape has no variant.
 cudaError_t launch_gemv(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs,
                         void* Y);
 cudaError_t launch_gemv_pair_swiglu(LaunchCtx& ctx, const void* A, const QWeight& gate,

@@ -155,6 +155,15 @@ MNB_API mnb_status mnb_gemv_gate_up_swiglu(const void *A, mnb_weight gate, mnb_w
  */
 MNB_API void mnb_set_programmatic_launch(int enable);
 
+/*
+ * Reads and clears the device status word. Kernels that wait on shared-memory barriers
+ * bound every wait; one that gives up sets a bit in this word, writes NaN outputs and
+ * returns instead of hanging. Returns MNB_ERR_TIMEOUT (with the bits in the message) if
+ * any bit was set since the last check, else MNB_OK. Synchronises the current device, so
+ * it must not be called while a stream is being captured.
+ */
+MNB_API mnb_status mnb_check_device_status(void);
+
 /* Message of the last failed call on this host thread ("" if none). */
 MNB_API const char *mnb_last_error(void);
 

@@ -60,7 +60,7 @@ def test_dequant_prefill_weight_bit_exact(env):
     assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("K,N,bs", [(64, 1, 16), (96, 130, 32), (256, 128, 64), (192, 257, 128),
+@pytest.mark.parametrize("K,N,bs", [(64, 1, 16), (96, 130, 32), (256, 128, 64), (192, 257, 64),
                                     (4096, 14336, 128)])
 def test_repack_bit_exact(env, K, N, bs):
     mnb, torch, dev = env
@@ -327,3 +327,30 @@ def test_programmatic_launch_gives_same_bits(env):
         mnb.mnb_set_programmatic_launch(False)
     for b, p in zip(base, pdl):
         assert torch.equal(b, p)
+
+
+@pytest.mark.parametrize("wname,variant", [("gemv_attnproj_k4096_n4096", "gemv_tma_ring"),
+                                           ("mlp_down_k14336_n4096", "gemv_tma_ring"),
+                                           ("tiny_gemv_k256_n128", "gemv_f16acc32")])
+def test_gemv_dispatch_picks_the_streaming_kernel(env, wname, variant):
+    mnb, torch, dev = env
+    wl = syn.WORKLOADS[wname]
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    mnb.mnb_gemv(upload_act(A.reshape(-1), dev), *upload_weight(w, dev), wl.K, wl.N, wl.block_size)
+    assert mnb.mnb_last_variant() == variant
+
+
+def test_swiglu_dispatch_picks_the_streaming_kernel(env):
+    mnb, torch, dev = env
+    wl = syn.WORKLOADS["mlp_gate_up_k4096_n14336"]
+    wg = upload_weight(syn.make_weight(wl, "gate"), dev)
+    wu = upload_weight(syn.make_weight(wl, "up"), dev)
+    a = upload_act(syn.make_activation(wl).reshape(-1), dev)
+    mnb.mnb_gemv_gate_up_swiglu(a, wg, wu, wl.K, wl.N, wl.block_size)
+    assert mnb.mnb_last_variant() == "gemv_pair_swiglu_tma_ring"
+
+
+def test_device_status_is_clean_after_the_suite(env):
+    mnb, torch, dev = env
+    mnb.mnb_check_device_status()
