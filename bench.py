@@ -388,6 +388,21 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_single(db, name, steps, warmup):
+    W = syn.WORKLOADS
+    if name == "attn":
+        return db.gemv(W[HEADLINE], steps, warmup, None)
+    if name == "gate_up":
+        return db.swiglu(W["mlp_gate_up_k4096_n14336"], steps, warmup, None)
+    if name == "down":
+        return db.gemv(W["mlp_down_k14336_n4096"], steps, warmup, None, calls=200)
+    if name.startswith("verify_m"):
+        return db.gemm(W[f"{name}_k4096_n4096"], steps, warmup, None, calls=200, repacked=False)
+    if name == "prefill":
+        return db.gemm(W["prefill_m2048_k4096_n14336"], steps, warmup, None, calls=9, repacked=True)
+    raise SystemExit(f"unknown workload {name}")
+
+
 # ---------------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
@@ -397,6 +412,9 @@ def main():
     ap.add_argument("--impl", default="mnb", choices=["mnb", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline only, short CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=None,
+                    help="time one workload only (attn, gate_up, down, verify_m2/4/8/16, prefill) "
+                         "and print its record; for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -426,6 +444,13 @@ def main():
     sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") if rank == 0 else None)
     db = DeviceBench(torch, mnb, dev, l2, rank)
     sampler.start()
+
+    if args.workload:
+        res = run_single(db, args.workload, args.steps, args.warmup)
+        sampler.stop()
+        if rank == 0:
+            print(json.dumps({k: v for k, v in res.items() if k not in ("graph", "A", "Y", "w", "buffers")}))
+        return
 
     wl = syn.WORKLOADS[HEADLINE]
     head = db.gemv(wl, args.steps, args.warmup, sampler)

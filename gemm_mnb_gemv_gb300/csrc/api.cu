@@ -10,7 +10,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/mnb.h"
+#include "mnb.h"
 #include "mnb_internal.h"
 
 namespace {

@@ -3,44 +3,44 @@
 // A CTA owns a contiguous range of output columns, so its packed weights, scales and
 // zero points are three contiguous byte ranges of the MatMulNBits storage.  One producer
 // lane streams them, a stage of CB columns at a time, with 1-D `cp.async.bulk` copies
-// into a ring of shared-memory slots (64-100 KB in flight per SM, independent of the
-// register budget).  Eight consumer warps keep their activations in registers, read each
+// into a ring of shared-memory slots (up to ~180 KB in flight per SM, independent of the
+// register budget).  NCW consumer warps keep their activations in registers, read each
 // stage's 16-byte weight chunks from shared memory, form exact fp16 (code - zp) with the
 // magic-number conversion, accumulate exact fp16 x fp16 products in fp32, apply the group
 // scale to each 32-element partial dot, and reduce per column in a fixed order.
 //
 // Warps are grouped: WG consumer warps cover one column's K range (lane slot s owns the
-// 32-element chunks s, s + 32 WG, ...), and 8 / WG groups work on different columns of a
-// stage.  Every wait on an mbarrier is bounded; a wait that gives up records its cause in
-// the device status word and the kernel finishes without further shared-memory traffic
-// (its outputs are then NaN).
+// 32-element chunks s, s + 32 WG, ...), and NCW / WG groups work on different columns of
+// a stage.  Every wait on an mbarrier is bounded; a wait that gives up records its cause
+// in the device status word and the kernel finishes without further shared-memory
+// traffic (its outputs are then NaN).
 //
 // The producer issues its copies before the programmatic-launch wait (the weights are
 // never written by the preceding kernel); consumers wait before reading A.
+//
+// The kernel is specialised on the scale dtype (S16) and on the presence of zero points
+// (ZP) so the inner loop carries no per-chunk branches on them; for the paired kernel
+// both weights must share those two properties.
 #include "mnb_device.cuh"
 #include "mnb_internal.h"
 
 namespace mnb {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxColsPerCta = 128;
 constexpr int kMaxStages = 8;
-constexpr int kRingBudget = 100 * 1024;
 
 struct TmaGemvArgs {
   const __half* A;
   const uint8_t* packed[2];
   const uint8_t* scales[2];
   const uint8_t* zp[2];
-  int scales_f16[2];
   void* Y;
   int K, N, G;
-  int group_shift;
-  int row_bytes;   // K / 2
-  int sbytes[2];   // scale bytes per row
-  int zbytes[2];   // zero-point bytes per row (0 when absent)
+  int group_shift;  // log2(bs / 32) for bs >= 32
+  int row_bytes;    // K / 2
+  int sbytes;       // scale bytes per row
+  int zbytes;       // zero-point bytes per row (0 when absent)
   int stage_bytes;
   int stages;
   uint32_t* status;
@@ -59,13 +59,17 @@ __device__ __forceinline__ float dot_word_tma(uint32_t w, uint32_t zlo, uint32_t
   return acc;
 }
 
-template <int WG, int CPS, int VPG, bool BS16, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 2) gemv_tma_kernel(const TmaGemvArgs p) {
-  constexpr int NG = kConsumerWarps / WG;
+template <int NCW, int WG, int CPS, int VPG, bool BS16, bool PAIR, bool S16, bool ZP>
+__global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
+    gemv_tma_kernel(const TmaGemvArgs p) {
+  constexpr int kThreads = (NCW + 1) * 32;
+  constexpr int NG = NCW / WG;
   constexpr int CB = NG * VPG;
   constexpr int NWT = PAIR ? 2 : 1;
   constexpr int V = VPG * NWT;
   constexpr int kLog2V = (V == 1) ? 0 : (V == 2) ? 1 : (V == 4) ? 2 : (V == 8) ? 3 : 4;
+  constexpr int kSB = S16 ? 2 : 4;  // bytes per scale
+  static_assert(NG * WG == NCW, "consumer warps must split into whole groups");
   static_assert(V <= 16, "too many values per lane");
 
   extern __shared__ __align__(128) uint8_t ring[];
@@ -82,65 +86,52 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tma_kernel(const TmaGemvArgs
   const int C = p.K >> 5;
 
   // Region offsets inside a stage: for each weight, packed | scales | zero points.
-  int off_p[NWT], off_s[NWT], off_z[NWT];
-  {
-    int off = 0;
-#pragma unroll
-    for (int t = 0; t < NWT; ++t) {
-      off_p[t] = off;
-      off += CB * p.row_bytes;
-      off_s[t] = off;
-      off += CB * p.sbytes[t];
-      off_z[t] = off;
-      off += CB * p.zbytes[t];
-    }
-  }
+  const int reg_p = CB * p.row_bytes, reg_s = CB * p.sbytes, reg_z = CB * p.zbytes;
+  const int wt_stride = reg_p + reg_s + reg_z;
 
   if (tid == 0) {
     failed = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kConsumerWarps);
+      mbar_init(&empty_bar[s], NCW);
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp == NCW) {
     // ------------------------------- producer -------------------------------------
-    int issued = 0;
     if (lane == 0) {
+      int issued = 0, slot = 0;
+      uint32_t phase = 0;
       for (int st = 0; st < nstages_total; ++st) {
-        const int slot = st % S;
-        const uint32_t round = (uint32_t)(st / S);
-        if (st >= S && !mbar_wait_bounded(&empty_bar[slot], (round - 1) & 1u)) {
+        if (st >= S && !mbar_wait_bounded(&empty_bar[slot], phase ^ 1u)) {
           report_status(p.status, kStatusEmptyWait);
           atomicExch(&failed, 1);
           break;
         }
         const int col = n0 + st * CB;
         const int nc = min(CB, n1 - col);
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int t = 0; t < NWT; ++t) bytes += (uint32_t)nc * (p.row_bytes + p.sbytes[t] + p.zbytes[t]);
+        const uint32_t bytes = (uint32_t)(nc * NWT) * (p.row_bytes + p.sbytes + p.zbytes);
         uint8_t* base = ring + (size_t)slot * p.stage_bytes;
         mbar_arrive_expect_tx(&full_bar[slot], bytes);
 #pragma unroll
         for (int t = 0; t < NWT; ++t) {
-          bulk_g2s(base + off_p[t], p.packed[t] + (long long)col * p.row_bytes, nc * p.row_bytes,
-                   &full_bar[slot]);
-          bulk_g2s(base + off_s[t], p.scales[t] + (long long)col * p.sbytes[t], nc * p.sbytes[t],
-                   &full_bar[slot]);
-          if (p.zbytes[t])
-            bulk_g2s(base + off_z[t], p.zp[t] + (long long)col * p.zbytes[t], nc * p.zbytes[t],
+          uint8_t* wb = base + t * wt_stride;
+          bulk_g2s(wb, p.packed[t] + (long long)col * p.row_bytes, nc * p.row_bytes, &full_bar[slot]);
+          bulk_g2s(wb + reg_p, p.scales[t] + (long long)col * p.sbytes, nc * p.sbytes, &full_bar[slot]);
+          if (ZP)
+            bulk_g2s(wb + reg_p + reg_s, p.zp[t] + (long long)col * p.zbytes, nc * p.zbytes,
                      &full_bar[slot]);
         }
         issued = st + 1;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
-    }
-    // Every copy this lane issued must land before the CTA can exit.  Consumers have
-    // normally waited for all of them already; after a failed wait this bounds the drain.
-    if (lane == 0) {
+      // Every copy this lane issued must land before the CTA can exit.  Consumers have
+      // normally waited for all of them already; after a failed wait this bounds the drain.
       for (int st = issued > S ? issued - S : 0; st < issued; ++st)
         (void)mbar_wait_bounded(&full_bar[st % S], (uint32_t)(st / S) & 1u);
     }
@@ -152,84 +143,88 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tma_kernel(const TmaGemvArgs
     const int g = warp / WG, wig = warp % WG;
     const int ls = wig * 32 + lane;
 
+    // Per owned chunk: activations (paired) and byte offsets, inside one column's
+    // regions, of its weights, its (first) scale and its zero-point byte.
     uint32_t a[CPS][16];
+    uint32_t wofs[CPS], sofs[CPS], zofs[CPS], zsh[CPS];
+    bool cval[CPS];
 #pragma unroll
     for (int j = 0; j < CPS; ++j) {
       const int c = ls + j * WG * 32;
+      cval[j] = c < C;
+      wofs[j] = (uint32_t)c * 16u;
+      const int gi = BS16 ? 2 * c : (c >> p.group_shift);
+      sofs[j] = (uint32_t)gi * kSB;
+      zofs[j] = BS16 ? (uint32_t)c : (uint32_t)(gi >> 1);
+      zsh[j] = BS16 ? 0u : (uint32_t)((gi & 1) * 4);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 x = make_uint4(0, 0, 0, 0);
-        if (c < C) x = *reinterpret_cast<const uint4*>(p.A + (long long)c * 32 + q * 8);
+        if (cval[j]) x = *reinterpret_cast<const uint4*>(p.A + (long long)c * 32 + q * 8);
         pair_halves_stride4(x, &a[j][q * 4]);
       }
     }
+    const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
+    const uint32_t ring_u32 = smem_u32(ring);
 
     bool ok = true;
+    int slot = 0;
+    uint32_t phase = 0;
     for (int st = 0; st < nstages_total; ++st) {
-      const int slot = st % S;
-      const uint32_t round = (uint32_t)(st / S);
-      if (ok && !mbar_wait_bounded(&full_bar[slot], round & 1u)) {
+      if (ok && !mbar_wait_bounded(&full_bar[slot], phase)) {
         report_status(p.status, kStatusFullWait);
         atomicExch(&failed, 1);
         ok = false;
       }
       const int col0 = n0 + st * CB;
       const int nc = min(CB, n1 - col0);
-      const uint8_t* base = ring + (size_t)slot * p.stage_bytes;
+      const uint32_t sb = ring_u32 + (uint32_t)(slot * p.stage_bytes);
       float part[V];
 #pragma unroll
       for (int vi = 0; vi < VPG; ++vi) {
         const int ci = g + vi * NG;
+        const bool live = ok && ci < nc;
 #pragma unroll
         for (int t = 0; t < NWT; ++t) {
           float acc = 0.0f;
-          if (ok && ci < nc) {
-            const uint8_t* pp = base + off_p[t] + ci * p.row_bytes;
-            const uint8_t* ps = base + off_s[t] + ci * p.sbytes[t];
-            const uint8_t* pz = base + off_z[t] + ci * p.zbytes[t];
+          const uint32_t cp = sb + (uint32_t)(t * wt_stride + ci * p.row_bytes);
+          const uint32_t cs = sb + (uint32_t)(t * wt_stride + reg_p + ci * p.sbytes);
+          const uint32_t cz = sb + (uint32_t)(t * wt_stride + reg_p + reg_s + ci * p.zbytes);
 #pragma unroll
-            for (int j = 0; j < CPS; ++j) {
-              const int c = ls + j * WG * 32;
-              if (c < C) {
-                const uint4 w4 = lds128(pp + c * 16);
-                if (BS16) {
-                  const uint32_t zb = p.zbytes[t] ? (uint32_t)pz[c] : 0x88u;
-                  const uint32_t z0 = zb & 15u, z1 = zb >> 4;
-                  const uint32_t zl0 = zp_lo_const(z0), zh0 = zp_hi_const(z0);
-                  const uint32_t zl1 = zp_lo_const(z1), zh1 = zp_hi_const(z1);
-                  float p0 = dot_word_tma(w4.x, zl0, zh0, &a[j][0], 0.0f);
-                  p0 = dot_word_tma(w4.y, zl0, zh0, &a[j][4], p0);
-                  float p1 = dot_word_tma(w4.z, zl1, zh1, &a[j][8], 0.0f);
-                  p1 = dot_word_tma(w4.w, zl1, zh1, &a[j][12], p1);
-                  float s0, s1;
-                  if (p.scales_f16[t]) {
-                    const __half* sh = reinterpret_cast<const __half*>(ps);
-                    s0 = __half2float(sh[2 * c]);
-                    s1 = __half2float(sh[2 * c + 1]);
-                  } else {
-                    const float* sf = reinterpret_cast<const float*>(ps);
-                    s0 = sf[2 * c];
-                    s1 = sf[2 * c + 1];
-                  }
-                  acc = fmaf(p0, s0, acc);
-                  acc = fmaf(p1, s1, acc);
+          for (int j = 0; j < CPS; ++j) {
+            if (live && cval[j]) {
+              const uint4 w4 = lds128_a(cp + wofs[j]);
+              const uint32_t zb = ZP ? lds_u8_a(cz + zofs[j]) : 0x88u;
+              if (BS16) {
+                const uint32_t z0 = zb & 15u, z1 = zb >> 4;
+                const uint32_t zl0 = ZP ? zp_lo_const(z0) : zl8, zh0 = ZP ? zp_hi_const(z0) : zh8;
+                const uint32_t zl1 = ZP ? zp_lo_const(z1) : zl8, zh1 = ZP ? zp_hi_const(z1) : zh8;
+                float p0 = dot_word_tma(w4.x, zl0, zh0, &a[j][0], 0.0f);
+                p0 = dot_word_tma(w4.y, zl0, zh0, &a[j][4], p0);
+                float p1 = dot_word_tma(w4.z, zl1, zh1, &a[j][8], 0.0f);
+                p1 = dot_word_tma(w4.w, zl1, zh1, &a[j][12], p1);
+                float s0, s1;
+                if (S16) {
+                  const uint32_t sh = lds_u32_a(cs + sofs[j]);
+                  s0 = half_bits_to_float(sh & 0xffffu);
+                  s1 = half_bits_to_float(sh >> 16);
                 } else {
-                  const int gi = c >> p.group_shift;
-                  uint32_t zz = 8u;
-                  if (p.zbytes[t]) {
-                    const uint32_t zb = pz[gi >> 1];
-                    zz = (gi & 1) ? (zb >> 4) : (zb & 15u);
-                  }
-                  const uint32_t zlo = zp_lo_const(zz), zhi = zp_hi_const(zz);
-                  float q0 = dot_word_tma(w4.x, zlo, zhi, &a[j][0], 0.0f);
-                  float q1 = dot_word_tma(w4.y, zlo, zhi, &a[j][4], 0.0f);
-                  q0 = dot_word_tma(w4.z, zlo, zhi, &a[j][8], q0);
-                  q1 = dot_word_tma(w4.w, zlo, zhi, &a[j][12], q1);
-                  const float s = p.scales_f16[t]
-                                      ? __half2float(reinterpret_cast<const __half*>(ps)[gi])
-                                      : reinterpret_cast<const float*>(ps)[gi];
-                  acc = fmaf(q0 + q1, s, acc);
+                  const uint2 sf = lds_u64_a(cs + sofs[j]);
+                  s0 = __uint_as_float(sf.x);
+                  s1 = __uint_as_float(sf.y);
                 }
+                acc = fmaf(p0, s0, acc);
+                acc = fmaf(p1, s1, acc);
+              } else {
+                const uint32_t zz = (zb >> zsh[j]) & 15u;
+                const uint32_t zlo = ZP ? zp_lo_const(zz) : zl8, zhi = ZP ? zp_hi_const(zz) : zh8;
+                float q0 = dot_word_tma(w4.x, zlo, zhi, &a[j][0], 0.0f);
+                float q1 = dot_word_tma(w4.y, zlo, zhi, &a[j][4], 0.0f);
+                q0 = dot_word_tma(w4.z, zlo, zhi, &a[j][8], q0);
+                q1 = dot_word_tma(w4.w, zlo, zhi, &a[j][12], q1);
+                const float s = S16 ? half_bits_to_float(lds_u16_a(cs + sofs[j]))
+                                    : __uint_as_float(lds_u32_a(cs + sofs[j]));
+                acc = fmaf(q0 + q1, s, acc);
               }
             }
           }
@@ -244,6 +239,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tma_kernel(const TmaGemvArgs
         const int vi = v / NWT, t = v % NWT;
         const int ci = g + vi * NG;
         if (ci < nc) red[wig][t][st * CB + ci] = r;
+      }
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
       }
     }
   }
@@ -268,23 +267,32 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_tma_kernel(const TmaGemvArgs
 // ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
-template <bool PAIR>
+// Sixteen consumer warps per CTA and one CTA per SM: enough warps per scheduler to keep
+// the conversion and FMA pipes issuing while the ring streams.
+constexpr int kNCW = 16;
+constexpr int kRingBudget = 180 * 1024;
+
 using TmaKernel = void (*)(const TmaGemvArgs);
 
 template <int WG, int CPS, bool PAIR>
-TmaKernel<PAIR> pick(bool bs16) {
+TmaKernel pick(bool bs16, bool s16, bool zp) {
   constexpr int VPG = PAIR ? 2 : 4;
-  return bs16 ? gemv_tma_kernel<WG, CPS, VPG, true, PAIR> : gemv_tma_kernel<WG, CPS, VPG, false, PAIR>;
+#define MNB_PICK(B, S, Z) gemv_tma_kernel<kNCW, WG, CPS, VPG, B, PAIR, S, Z>
+  if (bs16) {
+    if (s16) return zp ? MNB_PICK(true, true, true) : MNB_PICK(true, true, false);
+    return zp ? MNB_PICK(true, false, true) : MNB_PICK(true, false, false);
+  }
+  if (s16) return zp ? MNB_PICK(false, true, true) : MNB_PICK(false, true, false);
+  return zp ? MNB_PICK(false, false, true) : MNB_PICK(false, false, false);
+#undef MNB_PICK
 }
 
 template <bool PAIR>
-TmaKernel<PAIR> select_kernel(int wg, int cps, bool bs16) {
-  if (wg == 1) return pick<1, 1, PAIR>(bs16);
-  if (wg == 2) return pick<2, 1, PAIR>(bs16);
-  if (wg == 4) return pick<4, 1, PAIR>(bs16);
-  if (cps == 1) return pick<8, 1, PAIR>(bs16);
-  if (cps == 2) return pick<8, 2, PAIR>(bs16);
-  return pick<8, 4, PAIR>(bs16);
+TmaKernel select_kernel(int wg, int cps, bool bs16, bool s16, bool zp) {
+  if (wg == 4) return pick<4, 1, PAIR>(bs16, s16, zp);
+  if (cps == 1) return pick<8, 1, PAIR>(bs16, s16, zp);
+  if (cps == 2) return pick<8, 2, PAIR>(bs16, s16, zp);
+  return pick<8, 4, PAIR>(bs16, s16, zp);
 }
 
 template <bool PAIR>
@@ -292,15 +300,26 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
                             void* Y) {
   constexpr int NWT = PAIR ? 2 : 1;
   if (K % 32 != 0) return cudaErrorNotSupported;
+  if (PAIR && (w[0].scales_f16 != w[1].scales_f16 || (w[0].zp == nullptr) != (w[1].zp == nullptr)))
+    return cudaErrorNotSupported;
   const int C = K / 32;
-  int wg = 1;
-  while (wg < 8 && wg * 32 < C) wg *= 2;
-  int cps = (C + wg * 32 - 1) / (wg * 32);
-  if (cps == 3) cps = 4;
-  if (cps > 4) return cudaErrorNotSupported;
-  const int ng = kConsumerWarps / wg;
+  // Four warps cover K <= 4096 (one chunk per lane); eight warps with one, two or four
+  // chunks per lane cover K <= 32768.
+  int wg, cps;
+  if (C <= 128) {
+    wg = 4;
+    cps = 1;
+  } else {
+    wg = 8;
+    cps = (C + 255) / 256;
+    if (cps == 3) cps = 4;
+    if (cps > 4) return cudaErrorNotSupported;
+  }
+  const int ng = kNCW / wg;
   const int cb = ng * (PAIR ? 2 : 4);
   const int G = K / bs;
+  const bool s16 = w[0].scales_f16 != 0;
+  const bool zp = w[0].zp != nullptr;
   TmaGemvArgs a = {};
   a.A = static_cast<const __half*>(A);
   a.Y = Y;
@@ -310,21 +329,16 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   a.row_bytes = K / 2;
   a.group_shift = 0;
   while (bs >= 32 && (32 << a.group_shift) < bs) ++a.group_shift;
-  int col_bytes = 0;
+  a.sbytes = G * (s16 ? 2 : 4);
+  a.zbytes = zp ? (G + 1) / 2 : 0;
+  if (a.sbytes % 16 != 0 || a.zbytes % 16 != 0) return cudaErrorNotSupported;
   for (int t = 0; t < 2; ++t) {
     const QWeight& q = w[t < NWT ? t : 0];
     a.packed[t] = q.packed;
     a.scales[t] = static_cast<const uint8_t*>(q.scales);
     a.zp[t] = q.zp;
-    a.scales_f16[t] = q.scales_f16;
-    a.sbytes[t] = G * (q.scales_f16 ? 2 : 4);
-    a.zbytes[t] = q.zp ? (G + 1) / 2 : 0;
-    if (t < NWT) {
-      if (a.sbytes[t] % 16 != 0 || a.zbytes[t] % 16 != 0) return cudaErrorNotSupported;
-      col_bytes += a.row_bytes + a.sbytes[t] + a.zbytes[t];
-    }
   }
-  a.stage_bytes = cb * col_bytes;
+  a.stage_bytes = cb * NWT * (a.row_bytes + a.sbytes + a.zbytes);
   if (a.stage_bytes * 2 > kRingBudget) return cudaErrorNotSupported;
   a.stages = kRingBudget / a.stage_bytes;
   if (a.stages > kMaxStages) a.stages = kMaxStages;
@@ -334,11 +348,11 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   const int min_grid = (N + kMaxColsPerCta - 1) / kMaxColsPerCta;
   if (grid < min_grid) grid = min_grid;
   const size_t smem = (size_t)a.stages * a.stage_bytes;
-  auto kern = select_kernel<PAIR>(wg, cps, bs == 16);
+  auto kern = select_kernel<PAIR>(wg, cps, bs == 16, s16, zp);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ctx.variant = PAIR ? "gemv_pair_swiglu_tma_ring" : "gemv_tma_ring";
-  return launch_kernel(ctx, kern, dim3(grid), dim3(kThreads), smem, a);
+  return launch_kernel(ctx, kern, dim3(grid), dim3((kNCW + 1) * 32), smem, a);
 }
 
 }  // namespace

@@ -354,3 +354,20 @@ def test_swiglu_dispatch_picks_the_streaming_kernel(env):
 def test_device_status_is_clean_after_the_suite(env):
     mnb, torch, dev = env
     mnb.mnb_check_device_status()
+
+
+def test_gate_up_swiglu_weights_with_different_storage(env):
+    """Gate with fp16 scales and zero points, up with fp32 scales and none."""
+    mnb, torch, dev = env
+    wg_l = syn.custom("sw_mixed_gate", 1, 4096, 300, 64, scales_dtype="f16", has_zp=True)
+    wu_l = syn.custom("sw_mixed_up", 1, 4096, 300, 64, scales_dtype="f32", has_zp=False)
+    wg, wu = syn.make_weight(wg_l, "gate"), syn.make_weight(wu_l, "up")
+    A = syn.make_activation(wg_l)
+    out = mnb.mnb_gemv_gate_up_swiglu(upload_act(A.reshape(-1), dev), upload_weight(wg, dev),
+                                      upload_weight(wu, dev), 4096, 300, 64)
+    torch.cuda.synchronize()
+    ref, g, bg, u, bu = orc.gate_up_swiglu(A, (wg.packed, wg.scales, wg.zero_points),
+                                           (wu.packed, wu.scales, wu.zero_points), 4096, 300, 64)
+    tol = orc.swiglu_tolerance(g, bg, u, bu, ref)
+    got = out.cpu().numpy().astype(np.float64)[None, :]
+    assert np.all(np.abs(got - ref) <= tol)
