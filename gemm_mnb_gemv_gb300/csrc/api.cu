@@ -229,6 +229,9 @@ mnb_status mnb_gemm(const void* A, int M, mnb_weight w, const uint8_t* repacked,
   cudaError_t e;
   if (M == 1) {
     e = run_gemv(ctx, A, q, K, N, block_size, Y);
+  } else if (M > 16) {
+    e = mnb::launch_gemm_tc(ctx, A, M, q, repacked, K, N, block_size, Y);
+    if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, block_size, Y);
   } else {
     e = mnb::launch_generic(ctx, A, M, q, K, N, block_size, Y);
   }

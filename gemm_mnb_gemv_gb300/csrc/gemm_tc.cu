@@ -1,0 +1,387 @@
+// M > 16 GEMM on the tcgen05 tensor cores: Y[M,N] = A[M,K] . dequant(B)^T.
+//
+// Orientation: the dequantised weights are the MMA's A operand (M_mma = 128 weight rows,
+// i.e. 128 output columns n) and the activations are its B operand (N_mma = 256 rows m),
+// so the accumulator tile D[n, m] sits in TMEM with one weight row per TMEM lane.  The
+// per-group scale of row n is then a per-thread scalar in the epilogue, and "scale after
+// accumulate" (marlin_gemm.rs: per-group scaling applied after the tensor-core
+// accumulate) costs one FMA per accumulator element per group.
+//
+// Roles in a 512-thread CTA (one persistent CTA per SM, tiles of 128 n x 256 m):
+//   warp 0      producer: per 64-k stage, a 2-D TMA load of the 256 x 64 activation box
+//               (128-byte swizzle) and a 1-D bulk copy of the 4 KB repacked weight block;
+//   warp 1      MMA issuer (one lane) and TMEM owner (512 columns: two 256-column
+//               partial accumulators, one per quant group in flight);
+//   warps 4-7   dequantisers: repacked nibbles -> exact fp16 (code - zp) written into the
+//               K-major 128-byte-swizzled operand layout;
+//   warps 8-15  epilogue: per group, read the partial from TMEM, multiply by the group
+//               scale, add into fp32 registers; at the end of a tile, store fp16 Y.
+// Register split (setmaxnreg, warpgroup granularity, launch = 512 x 128):
+//   warpgroup 0: 40, warpgroup 1: 96, warpgroups 2-3: 184 -> 128 x (40+96+184+184) = 64512.
+// Every mbarrier wait is bounded; a wait that gives up sets the device status word and
+// the role stops, so the kernel always terminates.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "mnb_device.cuh"
+#include "mnb_internal.h"
+#include "tcgen05.cuh"
+
+namespace mnb {
+namespace {
+
+constexpr int kTileN = 128;  // weight rows per tile (M_mma)
+constexpr int kTileM = 256;  // activation rows per tile (N_mma)
+constexpr int kStageK = 64;
+constexpr int kStages = 4;
+constexpr int kXBytes = kTileM * kStageK * 2;   // 32 KB
+constexpr int kPBytes = kTileN * kStageK / 2;   // 4 KB
+constexpr int kWBytes = kTileN * kStageK * 2;   // 16 KB
+constexpr int kStageBytes = kXBytes + kPBytes + kWBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+constexpr int kThreads = 512;
+constexpr uint32_t kTmemCols = 512;
+
+struct TcArgs {
+  const uint8_t* repacked;
+  const uint8_t* scales;
+  const uint8_t* zp;
+  int scales_f16;
+  __half* Y;
+  int M, N, K, bs, G, zrb;
+  int kblocks;  // ceil(K / 64)
+  int mtiles, ntiles;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ uint32_t zp_byte(const TcArgs& p, int n, int byte_idx) {
+  if (p.zp == nullptr || n >= p.N || byte_idx >= p.zrb) return 0x88u;
+  return ld_nc_u8(p.zp + (long long)n * p.zrb + byte_idx);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const TcArgs p, const __grid_constant__ CUtensorMap tmap_a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kStages], wready_bar[kStages], empty_bar[kStages];
+  __shared__ uint64_t tfull_bar[2], tempty_bar[2], mma_done_bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const int KS = p.K / 16;                   // MMA k-steps per tile
+  const int ntile_total = p.mtiles * p.ntiles;
+
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&wready_bar[s], 4);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 8);
+    }
+    mbar_init(&mma_done_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  auto stage_x = [&](int s) { return smem + s * kStageBytes; };
+  auto stage_p = [&](int s) { return smem + s * kStageBytes + kXBytes; };
+  auto stage_w = [&](int s) { return smem + s * kStageBytes + kXBytes + kPBytes; };
+
+  const int wg = warp >> 2;
+  if (wg == 0) {
+    tc::setmaxnreg_dec<40>();
+    if (warp == 0 && lane == 0) {
+      // ------------------------------ producer ------------------------------------
+      tc::prefetch_tmap(&tmap_a);
+      pdl_launch_dependents();
+      pdl_wait();  // the activations may come from the previous kernel
+      int slot = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
+        const int mt = t % p.mtiles, nt = t / p.mtiles;
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (issued >= kStages && !mbar_wait_bounded(&empty_bar[slot], phase ^ 1u)) {
+            report_status(p.status, kStatusEmptyWait);
+            atomicExch(&abort_flag, 1);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[slot], kXBytes + kPBytes);
+          tc::tma_load_2d(stage_x(slot), &tmap_a, kb * kStageK, mt * kTileM, &full_bar[slot]);
+          bulk_g2s(stage_p(slot), p.repacked + ((long long)nt * p.kblocks + kb) * kPBytes, kPBytes,
+                   &full_bar[slot]);
+          ++issued;
+          if (++slot == kStages) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Let every copy land before the CTA can retire.
+      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+        (void)mbar_wait_bounded(&full_bar[i % kStages], (uint32_t)(i / kStages) & 1u);
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------ MMA issuer ----------------------------------
+      pdl_launch_dependents();
+      const uint32_t idesc = tc::idesc_f16_f32(kTileN, kTileM);
+      int slot = 0;
+      uint32_t phase = 0;
+      long long gc = 0;  // groups issued so far (selects the TMEM buffer)
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
+        for (int ks = 0; ks < KS && ok; ++ks) {
+          const int kk = ks & 3;
+          if (kk == 0) {
+            if (!mbar_wait_bounded(&full_bar[slot], phase) || !mbar_wait_bounded(&wready_bar[slot], phase)) {
+              report_status(p.status, kStatusMmaWait);
+              atomicExch(&abort_flag, 1);
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+          }
+          const bool first = ((ks * 16) % p.bs) == 0;
+          const bool last = (((ks + 1) * 16) % p.bs) == 0;
+          const uint32_t b = (uint32_t)(gc & 1);
+          if (first) {
+            if (gc >= 2 && !mbar_wait_bounded(&tempty_bar[b], (uint32_t)((gc >> 1) & 1) ^ 1u)) {
+              report_status(p.status, kStatusMmaWait);
+              atomicExch(&abort_flag, 1);
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+          }
+          const uint64_t ad = tc::smem_desc_k_sw128(smem_u32(stage_w(slot)) + kk * 32);
+          const uint64_t bd = tc::smem_desc_k_sw128(smem_u32(stage_x(slot)) + kk * 32);
+          tc::mma_f16(tmem + b * 256u, ad, bd, idesc, first ? 0u : 1u);
+          if (kk == 3 || ks == KS - 1) {
+            tc::mma_commit(&empty_bar[slot]);  // stage free once these MMAs complete
+            if (++slot == kStages) {
+              slot = 0;
+              phase ^= 1u;
+            }
+          }
+          if (last) {
+            tc::mma_commit(&tfull_bar[b]);
+            ++gc;
+          }
+        }
+      }
+      tc::mma_commit(&mma_done_bar);
+      (void)mbar_wait_bounded(&mma_done_bar, 0);
+    }
+  } else if (wg == 1) {
+    tc::setmaxnreg_dec<96>();
+    pdl_launch_dependents();
+    // ------------------------------ dequantisers -------------------------------------
+    const int r = tid - 128;  // weight row within the tile
+    int slot = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
+      const int nt = t / p.mtiles;
+      const int n = nt * kTileN + r;
+      // zero-point byte(s) for the first stage; later stages prefetch one stage ahead
+      auto zp_for = [&](int kb) -> uint32_t {
+        const int k0 = kb * kStageK;
+        if (p.bs == 16) return zp_byte(p, n, (k0 >> 4) >> 1) | (zp_byte(p, n, ((k0 >> 4) >> 1) + 1) << 8);
+        return zp_byte(p, n, (k0 / p.bs) >> 1);
+      };
+      uint32_t zcur = zp_for(0);
+      for (int kb = 0; kb < p.kblocks; ++kb) {
+        const uint32_t znext = (kb + 1 < p.kblocks) ? zp_for(kb + 1) : 0u;
+        if (!mbar_wait_bounded(&full_bar[slot], phase)) {
+          report_status(p.status, kStatusFullWait);
+          atomicExch(&abort_flag, 1);
+          ok = false;
+          break;
+        }
+        const uint8_t* sp = stage_p(slot);
+        uint8_t* sw = stage_w(slot);
+        const int k0 = kb * kStageK;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint4 v = lds128(sp + q * 2048 + r * 16);
+          const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int k = k0 + q * 32 + j * 8;  // first k of this word
+            uint32_t z;
+            if (p.bs == 16) {
+              const int gl = (k >> 4) - (k0 >> 4);  // 0..3 within the stage
+              z = (zcur >> (gl * 4)) & 15u;
+            } else {
+              const int g = k / p.bs;
+              z = (g & 1) ? ((zcur >> 4) & 15u) : (zcur & 15u);
+            }
+            uint32_t d[4];
+            nibbles_to_centered_half2(words[j], zp_lo_const(z), zp_hi_const(z), d);
+            const int c = q * 4 + j;  // 16-byte chunk (8 k) within the 128-byte row
+            *reinterpret_cast<uint4*>(sw + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(d[0], d[1], d[2], d[3]);
+          }
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wready_bar[slot]);
+        zcur = znext;
+        if (++slot == kStages) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    tc::setmaxnreg_inc<184>();
+    pdl_launch_dependents();
+    // ------------------------------ epilogue ----------------------------------------
+    const int e = warp - 8;          // 0..7
+    const int quarter = warp & 3;    // TMEM lanes 32*quarter .. +31
+    const int half = e >> 2;         // columns 128*half .. +127
+    long long gc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
+      const int mt = t % p.mtiles, nt = t / p.mtiles;
+      const int n = nt * kTileN + quarter * 32 + lane;
+      const bool nval = n < p.N;
+      float acc[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      auto scale_of = [&](int g) -> float {
+        if (!nval) return 0.0f;
+        const long long si = (long long)n * p.G + g;
+        return p.scales_f16 ? half_bits_to_float(ld_nc_u16(p.scales + 2 * si))
+                            : __uint_as_float(ld_nc_u32(p.scales + 4 * si));
+      };
+      float s_next = scale_of(0);
+      for (int g = 0; g < p.G; ++g) {
+        const float s = s_next;
+        if (g + 1 < p.G) s_next = scale_of(g + 1);
+        const uint32_t b = (uint32_t)(gc & 1);
+        if (!mbar_wait_bounded(&tfull_bar[b], (uint32_t)((gc >> 1) & 1))) {
+          report_status(p.status, kStatusMmaWait);
+          atomicExch(&abort_flag, 1);
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t tbase = tmem + b * 256u + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * 128);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tc::tmem_ld32(tbase + c * 32, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], s, acc[c * 32 + i]);
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[b]);
+        ++gc;
+      }
+      if (!ok) break;
+      if (nval) {
+        const int m0 = mt * kTileM + half * 128;
+        __half* yc = p.Y + n;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          const int m = m0 + i;
+          if (m < p.M) yc[(long long)m * p.N] = __float2half_rn(acc[i]);
+        }
+      }
+    }
+    if (abort_flag) {
+      // A wait gave up somewhere: mark this CTA's outputs as invalid.
+      for (int t = blockIdx.x; t < ntile_total; t += gridDim.x) {
+        const int mt = t % p.mtiles, nt = t / p.mtiles;
+        const int n = nt * kTileN + quarter * 32 + lane;
+        if (n >= p.N) continue;
+        for (int i = 0; i < 128; ++i) {
+          const int m = mt * kTileM + half * 128 + i;
+          if (m < p.M) p.Y[(long long)m * p.N + n] = __ushort_as_half(0x7e00);
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ----------------------------------------------------------------------------------
+// Host: tensor map for the activations (K innermost), cached driver entry point.
+// ----------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+size_t gemm_tc_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& w,
+                           const uint8_t* repacked, int K, int N, int bs, void* Y) {
+  if (K % 16 != 0) return cudaErrorNotSupported;
+  auto encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kStageK, (cuuint32_t)kTileM};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(A), gdim, gstride, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TcArgs a = {};
+  a.repacked = repacked;
+  a.scales = static_cast<const uint8_t*>(w.scales);
+  a.zp = w.zp;
+  a.scales_f16 = w.scales_f16;
+  a.Y = static_cast<__half*>(Y);
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bs = bs;
+  a.G = K / bs;
+  a.zrb = (a.G + 1) / 2;
+  a.kblocks = (K + kStageK - 1) / kStageK;
+  a.mtiles = (M + kTileM - 1) / kTileM;
+  a.ntiles = (N + kTileN - 1) / kTileN;
+  a.status = ctx.status;
+  const int tiles = a.mtiles * a.ntiles;
+  const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  ctx.variant = "gemm_tcgen05_w128xa256";
+  return launch_kernel(ctx, gemm_tc_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, a, tmap);
+}
+
+}  // namespace mnb

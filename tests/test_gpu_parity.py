@@ -166,11 +166,13 @@ def test_gemm_small_m_ragged(env, M, K, N, bs):
     assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
 
 
-@pytest.mark.parametrize("M,K,N,bs,sdt,zp", [(17, 128, 130, 32, "f16", True),
+@pytest.mark.parametrize("M,K,N,bs,sdt,zp", [(256, 128, 128, 128, "f16", True),
+                                             (17, 128, 130, 32, "f16", True),
                                              (64, 256, 256, 128, "f16", True),
                                              (200, 320, 384, 64, "f32", False),
                                              (300, 1024, 520, 16, "f16", True),
-                                             (256, 4096, 512, 128, "f16", True)])
+                                             (100, 96, 200, 32, "f32", True),
+                                             (513, 4096, 512, 128, "f16", True)])
 def test_gemm_large_m_ragged(env, M, K, N, bs, sdt, zp):
     mnb, torch, dev = env
     wl = syn.custom(f"lm_{M}_{K}_{N}_{bs}", M, K, N, bs, scales_dtype=sdt, has_zp=zp)
@@ -179,7 +181,9 @@ def test_gemm_large_m_ragged(env, M, K, N, bs, sdt, zp):
     packed, scales, zpt = upload_weight(w, dev)
     rp = mnb.mnb_repack(packed, K, N, bs)
     y = mnb.mnb_gemm(upload_act(A, dev), packed, scales, zpt, K, N, bs, repacked=rp)
+    assert mnb.mnb_last_variant() == "gemm_tcgen05_w128xa256"
     torch.cuda.synchronize()
+    mnb.mnb_check_device_status()
     Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
     assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
 
