@@ -17,7 +17,7 @@
 //   warps 8-15  epilogue: per group, read the partial from TMEM, multiply by the group
 //               scale, add into fp32 registers; at the end of a tile, store fp16 Y.
 // Register split (setmaxnreg, warpgroup granularity, launch = 512 x 128):
-//   warpgroup 0: 40, warpgroup 1: 96, warpgroups 2-3: 184 -> 128 x (40+96+184+184) = 64512.
+//   warpgroup 0: 64, warpgroup 1: 80, warpgroups 2-3: 184 -> 128 x (64+80+184+184) = 65536.
 // Every mbarrier wait is bounded; a wait that gives up sets the device status word and
 // the role stops, so the kernel always terminates.
 #include <cuda.h>
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int wg = warp >> 2;
   if (wg == 0) {
-    tc::setmaxnreg_dec<40>();
+    tc::setmaxnreg_dec<64>();
     if (warp == 0 && lane == 0) {
       // ------------------------------ producer ------------------------------------
       tc::prefetch_tmap(&tmap_a);
@@ -138,49 +138,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait_bounded(&full_bar[i % kStages], (uint32_t)(i / kStages) & 1u);
     } else if (warp == 1 && lane == 0) {
       // ------------------------------ MMA issuer ----------------------------------
+      // Kept to a few registers and no divisions: descriptors for slot 0 are built
+      // once and advanced by adding (byte offset >> 4) to their start-address field.
       pdl_launch_dependents();
       const uint32_t idesc = tc::idesc_f16_f32(kTileN, kTileM);
-      int slot = 0;
-      uint32_t phase = 0;
-      long long gc = 0;  // groups issued so far (selects the TMEM buffer)
+      const uint64_t dx0 = tc::smem_desc_k_sw128(smem_u32(smem));
+      const uint64_t dw0 = tc::smem_desc_k_sw128(smem_u32(smem) + kXBytes + kPBytes);
+      const uint32_t kpg_mask = (uint32_t)(p.bs / 16) - 1u;  // k-steps per group - 1
+      uint32_t slot = 0, phase = 0, b = 0, gphase = 0;
+      uint32_t ngroups = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
-        for (int ks = 0; ks < KS && ok; ++ks) {
-          const int kk = ks & 3;
-          if (kk == 0) {
-            if (!mbar_wait_bounded(&full_bar[slot], phase) || !mbar_wait_bounded(&wready_bar[slot], phase)) {
-              report_status(p.status, kStatusMmaWait);
-              atomicExch(&abort_flag, 1);
-              ok = false;
-              break;
-            }
-            tc::fence_after_sync();
+        uint32_t ks = 0;
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (!mbar_wait_bounded(&full_bar[slot], phase) || !mbar_wait_bounded(&wready_bar[slot], phase)) {
+            report_status(p.status, kStatusMmaWait);
+            atomicExch(&abort_flag, 1);
+            ok = false;
+            break;
           }
-          const bool first = ((ks * 16) % p.bs) == 0;
-          const bool last = (((ks + 1) * 16) % p.bs) == 0;
-          const uint32_t b = (uint32_t)(gc & 1);
-          if (first) {
-            if (gc >= 2 && !mbar_wait_bounded(&tempty_bar[b], (uint32_t)((gc >> 1) & 1) ^ 1u)) {
-              report_status(p.status, kStatusMmaWait);
-              atomicExch(&abort_flag, 1);
-              ok = false;
-              break;
+          tc::fence_after_sync();
+          const uint64_t off = (uint64_t)((slot * (uint32_t)kStageBytes) >> 4);
+          const uint32_t nk = min(4u, (uint32_t)KS - ks);
+#pragma unroll
+          for (uint32_t kk = 0; kk < 4; ++kk) {
+            if (kk < nk) {
+              const bool first = (ks & kpg_mask) == 0u;
+              if (first && ngroups >= 2u) {
+                if (!mbar_wait_bounded(&tempty_bar[b], gphase ^ 1u)) {
+                  report_status(p.status, kStatusMmaWait);
+                  atomicExch(&abort_flag, 1);
+                  ok = false;
+                  break;
+                }
+                tc::fence_after_sync();
+              }
+              tc::mma_f16(tmem + b * 256u, dw0 + off + 2u * kk, dx0 + off + 2u * kk, idesc, first ? 0u : 1u);
+              if ((ks & kpg_mask) == kpg_mask) {  // last k-step of the group
+                tc::mma_commit(&tfull_bar[b]);
+                ++ngroups;
+                b ^= 1u;
+                if (b == 0u) gphase ^= 1u;
+              }
+              ++ks;
             }
-            tc::fence_after_sync();
           }
-          const uint64_t ad = tc::smem_desc_k_sw128(smem_u32(stage_w(slot)) + kk * 32);
-          const uint64_t bd = tc::smem_desc_k_sw128(smem_u32(stage_x(slot)) + kk * 32);
-          tc::mma_f16(tmem + b * 256u, ad, bd, idesc, first ? 0u : 1u);
-          if (kk == 3 || ks == KS - 1) {
-            tc::mma_commit(&empty_bar[slot]);  // stage free once these MMAs complete
-            if (++slot == kStages) {
-              slot = 0;
-              phase ^= 1u;
-            }
-          }
-          if (last) {
-            tc::mma_commit(&tfull_bar[b]);
-            ++gc;
+          if (!ok) break;
+          tc::mma_commit(&empty_bar[slot]);  // stage free once these MMAs complete
+          if (++slot == (uint32_t)kStages) {
+            slot = 0;
+            phase ^= 1u;
           }
         }
       }
@@ -188,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (void)mbar_wait_bounded(&mma_done_bar, 0);
     }
   } else if (wg == 1) {
-    tc::setmaxnreg_dec<96>();
+    tc::setmaxnreg_dec<80>();
     pdl_launch_dependents();
     // ------------------------------ dequantisers -------------------------------------
     const int r = tid - 128;  // weight row within the tile
