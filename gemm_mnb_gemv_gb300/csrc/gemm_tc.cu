@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const TcArgs p, const __grid_constant__ CUtensorMap tmap_a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
-  __shared__ uint64_t wready_bar[kWBufs], wfree_bar[kWBufs];
+  __shared__ uint64_t wready_bar[kWBufs];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], mma_done_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -85,10 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int s = 0; s < kWBufs; ++s) {
-      mbar_init(&wready_bar[s], 4);
-      mbar_init(&wfree_bar[s], 1);
-    }
+    for (int s = 0; s < kWBufs; ++s) mbar_init(&wready_bar[s], 4);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
       mbar_init(&tempty_bar[b], 8);
@@ -158,7 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
         uint32_t ks = 0;
         for (int kb = 0; kb < p.kblocks && ok; ++kb) {
-          if (!mbar_spin_bounded(&full_bar[slot], phase) || !mbar_spin_bounded(&wready_bar[wb], wphase)) {
+          // The dequantisers arrive on wready only after observing this stage's full
+          // barrier (which also covers the activation box), so one wait orders both.
+          if (!mbar_spin_bounded(&wready_bar[wb], wphase)) {
             report_status(p.status, kStatusMmaWait);
             atomicExch(&abort_flag, 1);
             ok = false;
@@ -188,8 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_f16(d, aw + 4u, ax + 4u, idesc, 1u);
             tc::mma_f16(d, aw + 6u, ax + 6u, idesc, 1u);
             ks += 4u;
-            tc::mma_commit(&empty_bar[slot]);
-            tc::mma_commit(&wfree_bar[wb]);
+            tc::mma_commit(&empty_bar[slot]);  // ring slot and weight buffer free
             if (ends) {
               tc::mma_commit(&tfull_bar[b]);
               ++ngroups;
@@ -218,8 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ++ks;
             }
             if (!ok) break;
-            tc::mma_commit(&empty_bar[slot]);
-            tc::mma_commit(&wfree_bar[wb]);
+            tc::mma_commit(&empty_bar[slot]);  // ring slot and weight buffer free
           }
           if (++slot == (uint32_t)kStages) {
             slot = 0;
@@ -241,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     while ((1 << gshift) < p.bs) ++gshift;
     int slot = 0, wb = 0, si = 0;
     uint32_t phase = 0, wphase = 0;
+    int pslot = 0;          // ring slot of stage si - 2
+    uint32_t pphase = 0;    // parity of that slot's completed "empty" phase
     bool ok = true;
     const uint32_t w_u32 = smem_u32(smem) + kWOffset;
     for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
@@ -256,8 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t zcur = zp_for(0);
       for (int kb = 0; kb < p.kblocks; ++kb, ++si) {
         const uint32_t znext = (kb + 1 < p.kblocks) ? zp_for(kb + 1) : 0u;
+        // The weight buffer was last read by stage si - 2, whose completion is that
+        // stage's ring-slot "empty" phase.
         if (!mbar_wait_bounded(&full_bar[slot], phase) ||
-            (si >= kWBufs && !mbar_wait_bounded(&wfree_bar[wb], wphase ^ 1u))) {
+            (si >= kWBufs && !mbar_wait_bounded(&empty_bar[pslot], pphase))) {
           report_status(p.status, kStatusFullWait);
           atomicExch(&abort_flag, 1);
           ok = false;
@@ -270,14 +271,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 2; ++q) {
           const uint4 v = lds128(sp + q * 2048 + r * 16);
           const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+          // zero points of this 32-k half: one group for bs >= 32, two for bs = 16
+          const int gq = (kb * kStageK + q * 32) >> gshift;
+          uint32_t za, zb2;
+          if (gshift == 4) {
+            za = (zcur >> ((gq - g0) * 4)) & 15u;
+            zb2 = (zcur >> ((gq + 1 - g0) * 4)) & 15u;
+          } else {
+            za = (gq & 1) ? ((zcur >> 4) & 15u) : (zcur & 15u);
+            zb2 = za;
+          }
+          const uint32_t zla = zp_lo_const(za), zha = zp_hi_const(za);
+          const uint32_t zlb = zp_lo_const(zb2), zhb = zp_hi_const(zb2);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const int kin = q * 32 + j * 8;  // first k of this word within the stage
-            const int g = (kb * kStageK + kin) >> gshift;
-            const uint32_t z = (gshift == 4) ? ((zcur >> ((g - g0) * 4)) & 15u)
-                                             : ((g & 1) ? ((zcur >> 4) & 15u) : (zcur & 15u));
             uint32_t d[4];
-            nibbles_to_centered_half2(words[j], zp_lo_const(z), zp_hi_const(z), d);
+            nibbles_to_centered_half2(words[j], j < 2 ? zla : zlb, j < 2 ? zha : zhb, d);
             const int c = q * 4 + j;  // 16-byte chunk (8 k) within the 128-byte row
             asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(sw + (uint32_t)((c ^ (r & 7)) << 4)),
                          "r"(d[0]), "r"(d[1]), "r"(d[2]), "r"(d[3])
@@ -294,6 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         wb ^= 1;
         if (wb == 0) wphase ^= 1u;
+        if (si + 1 >= kWBufs + 1) {  // advance the (si - 2) cursor once si - 2 >= 0 was used
+          if (++pslot == kStages) {
+            pslot = 0;
+            pphase ^= 1u;
+          }
+        }
       }
     }
   } else {
