@@ -233,7 +233,8 @@ mnb_status mnb_gemm(const void* A, int M, mnb_weight w, const uint8_t* repacked,
     e = mnb::launch_gemm_tc(ctx, A, M, q, repacked, K, N, block_size, Y);
     if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, block_size, Y);
   } else {
-    e = mnb::launch_generic(ctx, A, M, q, K, N, block_size, Y);
+    e = mnb::launch_gemm_smallm(ctx, A, M, q, K, N, block_size, Y);
+    if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, block_size, Y);
   }
   return finish(fn, e, ctx);
 }

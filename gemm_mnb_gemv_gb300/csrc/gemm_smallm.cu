@@ -1,0 +1,294 @@
+// Speculative-verify GEMM, 2 <= M <= 16: Y[M,N] = A[M,K] . dequant(B)^T.
+//
+// HBM-bound (each weight is used M <= 16 times), so every weight byte is read once and
+// the dequantised values never touch shared memory: a CTA owns tiles of 16 weight rows,
+// a producer lane streams each tile (packed rows with a 16-byte row pad so the fragment
+// loads are bank-conflict free, plus the tile's scales and zero points) into a shared-
+// memory ring with 1-D bulk copies, and sixteen consumer warps in two groups of eight
+// work on two tiles at once, the eight warps of a group splitting K.  A lane converts
+// one 32-bit word (8 nibbles) of row g and of row g+8 into exact fp16 (code - zp) and
+// feeds them to two mma.sync.m16n8k16 (fp32 accumulate) as the A operand; the
+// activations, staged once per CTA in a fragment-ordered layout, are the B operand
+// (8 rows of A per instruction, two instructions per step for M > 8).
+//
+// The k index inside each MMA is permuted the same way for both operands: lane
+// (g, t) supplies physical k = 8t + {0,4,1,5} to the first MMA and 8t + {2,6,3,7} to the
+// second, which is exactly the pairing the magic-number conversion produces, so no
+// register shuffles are needed.  Each MMA spans one 32-k chunk, inside one quant group
+// for block sizes >= 32; per group the fresh fp32 fragment is multiplied by the group
+// scale of its row and added to the running sum (scale after accumulate, as in
+// matmul_nbits_marlin_gemm_f16 of marlin_gemm.rs).
+#include "mnb_device.cuh"
+#include "mnb_internal.h"
+
+namespace mnb {
+namespace {
+
+constexpr int kRows = 16;        // weight rows per tile
+constexpr int kCW = 16;          // consumer warps
+constexpr int kGroups = 2;       // tiles worked on at once (8 warps each)
+constexpr int kGW = kCW / kGroups;
+constexpr int kThreads = (kCW + 1) * 32;
+constexpr int kRowPad = 16;      // bytes between staged rows
+constexpr int kMaxStages = 4;
+constexpr int kSmemBudget = 200 * 1024;
+
+struct SmArgs {
+  const __half* A;
+  const uint8_t* packed;
+  const uint8_t* scales;
+  const uint8_t* zp;
+  __half* Y;
+  int M, K, N, G, gshift;
+  int row_bytes;     // K / 2
+  int srow;          // scale bytes per row
+  int zrow;          // zero-point bytes per row (0 if none)
+  int prow;          // staged row stride = row_bytes + kRowPad
+  int stage_bytes;   // kRows * prow + kRows * srow + kRows * zrow (16-aligned)
+  int stages;
+  int ntiles, tiles_per_cta;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");
+}
+__device__ __forceinline__ void group_bar(int gi) {
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + gi), "n"(kGW * 32) : "memory");
+}
+
+template <int MSETS, bool S16, bool ZP>
+__global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+  __shared__ float red[kGroups][kGW][MSETS][32][4];
+  __shared__ int failed;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = p.K >> 5;                 // 32-k chunks
+  const int S = p.stages;
+  // shared memory: [ring stages][activations in fragment order]
+  uint8_t* ring = smem_raw;
+  uint8_t* xs = smem_raw + (size_t)S * p.stage_bytes;
+  const int t_begin = blockIdx.x * p.tiles_per_cta;
+  const int t_end = min(p.ntiles, t_begin + p.tiles_per_cta);
+  const int ntile = t_end - t_begin;
+
+  if (tid == 0) {
+    failed = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kGW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kCW) {
+    // ------------------------------ producer ------------------------------------
+    if (lane == 0) {
+      int slot = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int i = 0; i < ntile; ++i) {
+        if (issued >= S && !mbar_wait_bounded(&empty_bar[slot], phase ^ 1u)) {
+          report_status(p.status, kStatusEmptyWait);
+          atomicExch(&failed, 1);
+          break;
+        }
+        const int n0 = (t_begin + i) * kRows;
+        const int nr = min(kRows, p.N - n0);
+        uint8_t* st = ring + (size_t)slot * p.stage_bytes;
+        const uint32_t bytes = (uint32_t)nr * (p.row_bytes + p.srow + p.zrow);
+        mbar_arrive_expect_tx(&full_bar[slot], bytes);
+        for (int r = 0; r < nr; ++r)
+          bulk_g2s(st + r * p.prow, p.packed + (long long)(n0 + r) * p.row_bytes, p.row_bytes, &full_bar[slot]);
+        bulk_g2s(st + kRows * p.prow, p.scales + (long long)n0 * p.srow, nr * p.srow, &full_bar[slot]);
+        if (ZP)
+          bulk_g2s(st + kRows * (p.prow + p.srow), p.zp + (long long)n0 * p.zrow, nr * p.zrow, &full_bar[slot]);
+        ++issued;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+        (void)mbar_wait_bounded(&full_bar[i % S], (uint32_t)(i / S) & 1u);
+    }
+    pdl_launch_dependents();
+  } else {
+    // ------------------------------ consumers -----------------------------------
+    pdl_launch_dependents();
+    pdl_wait();
+    // Stage the activations once: entry (set s, chunk c, lane l = 4g + t) holds
+    // A[8s + g][32c + 8t .. +8], paired (x0,x4)(x1,x5)(x2,x6)(x3,x7).
+    const int entries = MSETS * C * 32;
+    for (int e = tid; e < entries; e += kCW * 32) {
+      const int l = e & 31, c = (e >> 5) % C, s = (e >> 5) / C;
+      const int m = 8 * s + (l >> 2), k = 32 * c + 8 * (l & 3);
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (m < p.M) x = *reinterpret_cast<const uint4*>(p.A + (long long)m * p.K + k);
+      uint32_t q[4];
+      pair_halves_stride4(x, q);
+      *reinterpret_cast<uint4*>(xs + (size_t)e * 16) = make_uint4(q[0], q[1], q[2], q[3]);
+    }
+    consumer_bar();
+
+    const int g = lane >> 2, t = lane & 3;
+    const int gi = warp / kGW, gw = warp % kGW;  // tile group, warp within it
+    const int c_lo = (gw * C) / kGW, c_hi = ((gw + 1) * C) / kGW;
+    const uint32_t xs_u32 = smem_u32(xs);
+    const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
+    bool ok = true;
+    for (int i = gi; i < ntile; i += kGroups) {
+      const int slot = i % S;
+      const uint32_t phase = (uint32_t)(i / S) & 1u;
+      if (ok && !mbar_wait_bounded(&full_bar[slot], phase)) {
+        report_status(p.status, kStatusFullWait);
+        atomicExch(&failed, 1);
+        ok = false;
+      }
+      const uint32_t st = smem_u32(ring + (size_t)slot * p.stage_bytes);
+      const uint32_t rowg = st + (uint32_t)(g * p.prow) + 4u * t;
+      const uint32_t rowg8 = st + (uint32_t)((g + 8) * p.prow) + 4u * t;
+      const uint32_t sbase = st + (uint32_t)(kRows * p.prow);
+      const uint32_t zbase = sbase + (uint32_t)(kRows * p.srow);
+      // Two independent MMA chains per set (first and second half of each chunk's k).
+      float acc[MSETS][4], tmp[MSETS][4], tmp2[MSETS][4];
+#pragma unroll
+      for (int s = 0; s < MSETS; ++s)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[s][j] = tmp[s][j] = tmp2[s][j] = 0.0f;
+      int cur = -1;  // current group
+      uint32_t zlg = zl8, zhg = zh8, zlg8 = zl8, zhg8 = zh8;
+      float sg = 0.0f, sg8 = 0.0f;
+      auto flush = [&]() {
+#pragma unroll
+        for (int s = 0; s < MSETS; ++s) {
+          acc[s][0] = fmaf(tmp[s][0] + tmp2[s][0], sg, acc[s][0]);
+          acc[s][1] = fmaf(tmp[s][1] + tmp2[s][1], sg, acc[s][1]);
+          acc[s][2] = fmaf(tmp[s][2] + tmp2[s][2], sg8, acc[s][2]);
+          acc[s][3] = fmaf(tmp[s][3] + tmp2[s][3], sg8, acc[s][3]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tmp[s][j] = tmp2[s][j] = 0.0f;
+        }
+      };
+      if (ok) {
+        for (int c = c_lo; c < c_hi; ++c) {
+          const int grp = (c * 32) >> p.gshift;
+          if (grp != cur) {
+            if (cur >= 0) flush();
+            cur = grp;
+            if (S16) {
+              sg = half_bits_to_float(lds_u16_a(sbase + (uint32_t)(g * p.srow + 2 * grp)));
+              sg8 = half_bits_to_float(lds_u16_a(sbase + (uint32_t)((g + 8) * p.srow + 2 * grp)));
+            } else {
+              sg = __uint_as_float(lds_u32_a(sbase + (uint32_t)(g * p.srow + 4 * grp)));
+              sg8 = __uint_as_float(lds_u32_a(sbase + (uint32_t)((g + 8) * p.srow + 4 * grp)));
+            }
+            if (ZP) {
+              const uint32_t sh = (uint32_t)(grp & 1) * 4u;
+              const uint32_t z0 = (lds_u8_a(zbase + (uint32_t)(g * p.zrow + (grp >> 1))) >> sh) & 15u;
+              const uint32_t z1 = (lds_u8_a(zbase + (uint32_t)((g + 8) * p.zrow + (grp >> 1))) >> sh) & 15u;
+              zlg = zp_lo_const(z0);
+              zhg = zp_hi_const(z0);
+              zlg8 = zp_lo_const(z1);
+              zhg8 = zp_hi_const(z1);
+            }
+          }
+          const uint32_t wa = lds_u32_a(rowg + 16u * c);
+          const uint32_t wb = lds_u32_a(rowg8 + 16u * c);
+          uint32_t da[4], db[4];
+          nibbles_to_centered_half2(wa, zlg, zhg, da);
+          nibbles_to_centered_half2(wb, zlg8, zhg8, db);
+#pragma unroll
+          for (int s = 0; s < MSETS; ++s) {
+            const uint4 xf = lds128_a(xs_u32 + (uint32_t)(((s * C + c) * 32 + lane) * 16));
+            mma16816(tmp[s], da[0], db[0], da[1], db[1], xf.x, xf.y);
+            mma16816(tmp2[s], da[2], db[2], da[3], db[3], xf.z, xf.w);
+          }
+        }
+        if (cur >= 0) flush();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[slot]);
+#pragma unroll
+      for (int s = 0; s < MSETS; ++s)
+        *reinterpret_cast<float4*>(&red[gi][gw][s][lane][0]) = make_float4(acc[s][0], acc[s][1], acc[s][2], acc[s][3]);
+      group_bar(gi);
+      // Fixed-order sum over the K slices; one thread per (row, m).
+      const int n0 = (t_begin + i) * kRows;
+      for (int e = gw * 32 + lane; e < kRows * 8 * MSETS; e += kGW * 32) {
+        const int row = e % kRows, m = e / kRows;
+        const int s = m >> 3, mm = m & 7;
+        const int l = (row & 7) * 4 + (mm >> 1), j = ((row >> 3) << 1) + (mm & 1);
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kGW; ++w) v += red[gi][w][s][l][j];
+        const int n = n0 + row;
+        if (m < p.M && n < p.N) {
+          if (failed) v = __int_as_float(0x7fc00000);
+          p.Y[(long long)m * p.N + n] = __float2half_rn(v);
+        }
+      }
+      group_bar(gi);
+    }
+  }
+}
+
+using SmKernel = void (*)(const SmArgs);
+
+template <int MSETS>
+SmKernel pick(bool s16, bool zp) {
+  if (s16) return zp ? gemm_smallm_kernel<MSETS, true, true> : gemm_smallm_kernel<MSETS, true, false>;
+  return zp ? gemm_smallm_kernel<MSETS, false, true> : gemm_smallm_kernel<MSETS, false, false>;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
+                               void* Y) {
+  if (M < 2 || M > 16 || bs < 32 || K % 32 != 0) return cudaErrorNotSupported;
+  SmArgs a = {};
+  a.A = static_cast<const __half*>(A);
+  a.packed = w.packed;
+  a.scales = static_cast<const uint8_t*>(w.scales);
+  a.zp = w.zp;
+  a.Y = static_cast<__half*>(Y);
+  a.M = M;
+  a.K = K;
+  a.N = N;
+  a.G = K / bs;
+  a.gshift = 0;
+  while ((1 << a.gshift) < bs) ++a.gshift;
+  a.row_bytes = K / 2;
+  a.srow = a.G * (w.scales_f16 ? 2 : 4);
+  a.zrow = w.zp ? (a.G + 1) / 2 : 0;
+  if (a.srow % 16 != 0 || a.zrow % 16 != 0) return cudaErrorNotSupported;
+  a.prow = a.row_bytes + kRowPad;
+  a.stage_bytes = kRows * (a.prow + a.srow + a.zrow);
+  const int msets = M <= 8 ? 1 : 2;
+  const size_t xbytes = (size_t)msets * (K / 32) * 32 * 16;
+  if ((size_t)kSmemBudget < xbytes + 2 * (size_t)a.stage_bytes) return cudaErrorNotSupported;
+  a.stages = (int)((kSmemBudget - xbytes) / a.stage_bytes);
+  if (a.stages > kMaxStages) a.stages = kMaxStages;
+  a.ntiles = (N + kRows - 1) / kRows;
+  a.tiles_per_cta = (a.ntiles + ctx.num_sms - 1) / ctx.num_sms;
+  const int grid = (a.ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta;
+  a.status = ctx.status;
+  const size_t smem = (size_t)a.stages * a.stage_bytes + xbytes;
+  SmKernel kern = msets == 1 ? pick<1>(w.scales_f16 != 0, w.zp != nullptr) : pick<2>(w.scales_f16 != 0, w.zp != nullptr);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  ctx.variant = "gemm_smallm_mma16816";
+  return launch_kernel(ctx, kern, dim3(grid), dim3(kThreads), smem, a);
+}
+
+}  // namespace mnb

@@ -36,6 +36,9 @@ cudaError_t launch_gemv(LaunchCtx& ctx, const void* A, const QWeight& w, int K, 
                         void* Y);
 cudaError_t launch_gemv_pair_swiglu(LaunchCtx& ctx, const void* A, const QWeight& gate,
                                     const QWeight& up, int K, int N, int bs, void* out);
+// 2 <= M <= 16 (block size >= 32): weights streamed once, mma.sync over M rows.
+cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
+                               void* Y);
 // M > 16 on the tcgen05 tensor cores, reading the repacked operand.
 cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& w,
                            const uint8_t* repacked, int K, int N, int bs, void* Y);

@@ -148,20 +148,26 @@ def test_gemm_small_m_workloads_full_size(env, M):
     w = syn.make_weight(wl)
     A = syn.make_activation(wl)
     y = mnb.mnb_gemm(upload_act(A, dev), *upload_weight(w, dev), wl.K, wl.N, wl.block_size)
+    assert mnb.mnb_last_variant() == "gemm_smallm_mma16816"
     torch.cuda.synchronize()
+    mnb.mnb_check_device_status()
     Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size)
     assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
 
 
-@pytest.mark.parametrize("M,K,N,bs", [(3, 96, 130, 32), (5, 192, 200, 64), (13, 384, 77, 128),
-                                      (7, 48, 33, 16), (16, 1024, 129, 16)])
-def test_gemm_small_m_ragged(env, M, K, N, bs):
+@pytest.mark.parametrize("M,K,N,bs,sdt,zp", [(3, 96, 130, 32, "f16", True), (5, 192, 200, 64, "f16", True),
+                                             (13, 384, 77, 128, "f16", True), (7, 48, 33, 16, "f16", True),
+                                             (16, 1024, 129, 16, "f16", True),
+                                             (2, 1024, 300, 32, "f16", True), (9, 2048, 131, 64, "f32", False),
+                                             (16, 4096, 48, 128, "f32", True), (8, 8192, 100, 256 // 2, "f16", False)])
+def test_gemm_small_m_ragged(env, M, K, N, bs, sdt, zp):
     mnb, torch, dev = env
-    wl = syn.custom(f"sm_{M}_{K}_{N}_{bs}", M, K, N, bs)
+    wl = syn.custom(f"sm_{M}_{K}_{N}_{bs}", M, K, N, bs, scales_dtype=sdt, has_zp=zp)
     w = syn.make_weight(wl)
     A = syn.make_activation(wl)
     y = mnb.mnb_gemm(upload_act(A, dev), *upload_weight(w, dev), K, N, bs)
     torch.cuda.synchronize()
+    mnb.mnb_check_device_status()
     Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
     assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
 
