@@ -242,6 +242,32 @@ class DeviceBench:
         return {"workload": wl.name, "us_per_call": us, "gbps": call_bytes(wl, 2) / (us * 1e3),
                 "copies": ncopy, "variant": mnb.mnb_last_variant()}
 
+    def mlp_chain(self, steps, warmup, sampler, calls=100):
+        """Decode MLP at M = 1: gate/up SwiGLU GEMV feeding the down GEMV, one graph segment."""
+        torch, mnb = self.torch, self.mnb
+        wg = syn.WORKLOADS["mlp_gate_up_k4096_n14336"]
+        wd = syn.WORKLOADS["mlp_down_k14336_n4096"]
+        per = 2 * weight_bytes(wg) + weight_bytes(wd)
+        ncopy = self.copies_for(per)
+        _, gates = self.upload_weights(wg, "gate", ncopy)
+        _, ups = self.upload_weights(wg, "up", ncopy)
+        _, downs = self.upload_weights(wd, "B", ncopy)
+        x = torch.from_numpy(syn.make_activation(wg).reshape(-1)).to(self.dev)
+        h = torch.empty(wg.N, dtype=torch.float16, device=self.dev)
+        y = torch.empty(wd.N, dtype=torch.float16, device=self.dev)
+
+        def rec():
+            for i in range(calls):
+                j = i % ncopy
+                mnb.mnb_gemv_gate_up_swiglu(x, gates[j], ups[j], wg.K, wg.N, wg.block_size, out=h)
+                mnb.mnb_gemv(h, *downs[j], wd.K, wd.N, wd.block_size, out=y)
+
+        ms, _ = self.time_graph(rec, 2 * calls, steps, warmup, sampler)
+        us = ms * 1e3 / calls
+        nbytes = 2 * weight_bytes(wg) + weight_bytes(wd) + 2 * wg.K + 2 * wg.N + 2 * wd.N
+        return {"workload": "mlp_chain_gate_up_k4096_n14336_down", "us_per_call": us,
+                "gbps": nbytes / (us * 1e3), "copies": ncopy, "variant": "gate_up_swiglu + down gemv"}
+
     def gemm(self, wl, steps, warmup, sampler, calls, repacked: bool):
         torch, mnb = self.torch, self.mnb
         per_copy = weight_bytes(wl) + wl.M * wl.K * 2
@@ -398,6 +424,8 @@ def run_single(db, name, steps, warmup):
         return db.gemv(W["mlp_down_k14336_n4096"], steps, warmup, None, calls=200)
     if name.startswith("verify_m"):
         return db.gemm(W[f"{name}_k4096_n4096"], steps, warmup, None, calls=200, repacked=False)
+    if name == "mlp_chain":
+        return db.mlp_chain(steps, warmup, None)
     if name == "prefill":
         return db.gemm(W["prefill_m2048_k4096_n14336"], steps, warmup, None, calls=9, repacked=True)
     raise SystemExit(f"unknown workload {name}")
@@ -467,6 +495,7 @@ def main():
                                              calls=200, repacked=False)
         extras["prefill"] = db.gemm(syn.WORKLOADS["prefill_m2048_k4096_n14336"], 10, 3, sampler,
                                     calls=9, repacked=True)
+        extras["mlp_chain"] = db.mlp_chain(10, 3, sampler)
     for k, v in extras.items():
         log(f"{k}: {v['us_per_call']:.3f} us/call, {v.get('gbps', 0):.1f} GB/s, "
             f"{v.get('tflops', 0):.1f} TFLOP/s ({v['variant']})")

@@ -8,7 +8,8 @@ output tensor is not passed, the binding allocates it with torch before the call
 
 The names match the C entry points: ``mnb_dequant``, ``mnb_repacked_bytes``,
 ``mnb_repack``, ``mnb_gemv``, ``mnb_workspace_bytes``, ``mnb_gemm``,
-``mnb_gemv_gate_up_swiglu``, ``mnb_set_programmatic_launch``, ``mnb_check_device_status``,
+``mnb_gemm_bias``, ``mnb_gemv_gate_up_swiglu``, ``mnb_set_programmatic_launch``,
+``mnb_check_device_status``,
 ``mnb_last_error``,
 ``mnb_last_variant``, ``mnb_version``.
 """
@@ -60,6 +61,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mnb_workspace_bytes": (c_size, [c_int, c_int, c_int, c_int]),
         "mnb_gemm": (c_int, [vp, c_int, MnbWeight, vp, c_int, c_int, c_int, vp, c_size, vp, vp]),
         "mnb_gemv_gate_up_swiglu": (c_int, [vp, MnbWeight, MnbWeight, c_int, c_int, c_int, vp, vp]),
+        "mnb_gemm_bias": (c_int, [vp, c_int, MnbWeight, vp, c_int, c_int, c_int, vp, c_int, vp, c_size, vp, vp]),
         "mnb_set_programmatic_launch": (None, [c_int]),
         "mnb_check_device_status": (c_int, []),
         "mnb_last_error": (ctypes.c_char_p, []),
@@ -208,6 +210,31 @@ def mnb_gemm(A, packed, scales, zero_points, K: int, N: int, block_size: int, re
     _check_dev("out", out, torch.float16)
     _raise(lib.mnb_gemm(_ptr(A), M, w, _ptr(repacked), K, N, block_size, _ptr(workspace), ws_bytes,
                         _ptr(out), _stream_handle(stream)))
+    return out
+
+
+MNB_BIAS_NONE, MNB_BIAS_FUSED, MNB_BIAS_AFTER_ROUND = 0, 1, 2
+
+
+def mnb_gemm_bias(A, packed, scales, zero_points, K: int, N: int, block_size: int, bias, bias_mode: int,
+                  repacked=None, workspace=None, out=None, stream=None):
+    """``mnb_gemm`` plus a fp16 ``[N]`` bias: mode 1 = fp16(acc + b), mode 2 = fp16(fp16(acc) + b)."""
+    torch = _torch()
+    lib = load_library()
+    _check_dev("A", A, torch.float16)
+    _check_dev("bias", bias, torch.float16)
+    M = A.numel() // K
+    w = _weight(packed, scales, zero_points)
+    _check_dev("repacked", repacked, torch.uint8)
+    need = mnb_workspace_bytes(M, K, N, block_size)
+    if workspace is None and need > 0:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=A.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check_dev("out", out, torch.float16)
+    _raise(lib.mnb_gemm_bias(_ptr(A), M, w, _ptr(repacked), K, N, block_size, _ptr(bias), bias_mode,
+                             _ptr(workspace), ws_bytes, _ptr(out), _stream_handle(stream)))
     return out
 
 

@@ -206,10 +206,13 @@ size_t mnb_workspace_bytes(int M, int K, int N, int block_size) {
   return 0;
 }
 
-mnb_status mnb_gemm(const void* A, int M, mnb_weight w, const uint8_t* repacked, int K, int N,
-                    int block_size, void* workspace, size_t ws_bytes, void* Y,
-                    mnb_stream stream) {
-  const char* fn = "mnb_gemm";
+}  // extern "C"
+
+namespace {
+
+mnb_status gemm_impl(const char* fn, const void* A, int M, mnb_weight w, const uint8_t* repacked, int K, int N,
+                     int block_size, const void* bias, int bias_mode, void* workspace, size_t ws_bytes, void* Y,
+                     mnb_stream stream) {
   mnb_status st;
   mnb::QWeight q;
   if ((st = check_shape(fn, K, N, block_size)) != MNB_OK) return st;
@@ -224,8 +227,13 @@ mnb_status mnb_gemm(const void* A, int M, mnb_weight w, const uint8_t* repacked,
   if (M > 16) {
     if ((st = check_ptr(fn, "repacked", repacked)) != MNB_OK) return st;
   }
+  if (bias_mode < 0 || bias_mode > 2)
+    return fail(MNB_ERR_INVALID_ARG, "%s: bias_mode %d must be 0, 1 or 2", fn, bias_mode);
+  if (bias_mode != 0 && (st = check_ptr(fn, "bias", bias)) != MNB_OK) return st;
   mnb::LaunchCtx ctx;
   if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
+  ctx.bias = bias_mode ? bias : nullptr;
+  ctx.bias_mode = bias_mode;
   cudaError_t e;
   if (M == 1) {
     e = run_gemv(ctx, A, q, K, N, block_size, Y);
@@ -237,6 +245,24 @@ mnb_status mnb_gemm(const void* A, int M, mnb_weight w, const uint8_t* repacked,
     if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, block_size, Y);
   }
   return finish(fn, e, ctx);
+}
+
+}  // namespace
+
+extern "C" {
+
+mnb_status mnb_gemm(const void* A, int M, mnb_weight w, const uint8_t* repacked, int K, int N,
+                    int block_size, void* workspace, size_t ws_bytes, void* Y,
+                    mnb_stream stream) {
+  return gemm_impl("mnb_gemm", A, M, w, repacked, K, N, block_size, nullptr, 0, workspace, ws_bytes, Y,
+                   stream);
+}
+
+mnb_status mnb_gemm_bias(const void* A, int M, mnb_weight w, const uint8_t* repacked, int K, int N,
+                         int block_size, const void* bias, int bias_mode, void* workspace, size_t ws_bytes,
+                         void* Y, mnb_stream stream) {
+  return gemm_impl("mnb_gemm_bias", A, M, w, repacked, K, N, block_size, bias, bias_mode, workspace,
+                   ws_bytes, Y, stream);
 }
 
 mnb_status mnb_gemv_gate_up_swiglu(const void* A, mnb_weight gate, mnb_weight up, int K, int N,

@@ -48,6 +48,8 @@ struct SmArgs {
   int stages;
   int ntiles, tiles_per_cta;
   uint32_t* status;
+  const __half* bias;
+  int bias_mode;
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -234,8 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
         for (int w = 0; w < kGW; ++w) v += red[gi][w][s][l][j];
         const int n = n0 + row;
         if (m < p.M && n < p.N) {
-          if (failed) v = __int_as_float(0x7fc00000);
-          p.Y[(long long)m * p.N + n] = __float2half_rn(v);
+          p.Y[(long long)m * p.N + n] = failed ? __ushort_as_half(0x7e00) : round_out(v, p.bias, n, p.bias_mode);
         }
       }
       group_bar(gi);
@@ -283,6 +284,8 @@ cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeig
   a.tiles_per_cta = (a.ntiles + ctx.num_sms - 1) / ctx.num_sms;
   const int grid = (a.ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta;
   a.status = ctx.status;
+  a.bias = static_cast<const __half*>(ctx.bias);
+  a.bias_mode = ctx.bias_mode;
   const size_t smem = (size_t)a.stages * a.stage_bytes + xbytes;
   SmKernel kern = msets == 1 ? pick<1>(w.scales_f16 != 0, w.zp != nullptr) : pick<2>(w.scales_f16 != 0, w.zp != nullptr);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -57,6 +57,8 @@ struct TcArgs {
   int kblocks;  // ceil(K / 64)
   int mtiles, ntiles;
   uint32_t* status;
+  const __half* bias;
+  int bias_mode;
 };
 
 __device__ __forceinline__ uint32_t zp_byte(const TcArgs& p, int n, int byte_idx) {
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 128; ++i) {
           const int m = m0 + i;
-          if (m < p.M) yc[(long long)m * p.N] = __float2half_rn(acc[i]);
+          if (m < p.M) yc[(long long)m * p.N] = round_out(acc[i], p.bias, n, p.bias_mode);
         }
       }
     }
@@ -440,6 +442,8 @@ cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& 
   a.mtiles = (M + kTileM - 1) / kTileM;
   a.ntiles = (N + kTileN - 1) / kTileN;
   a.status = ctx.status;
+  a.bias = static_cast<const __half*>(ctx.bias);
+  a.bias_mode = ctx.bias_mode;
   const int tiles = a.mtiles * a.ntiles;
   const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);

@@ -38,6 +38,8 @@ struct GemvArgs {
   void* Y;
   int K, N, G, zrb;
   int group_shift;  // log2(bs / 32) when bs >= 32
+  const __half* bias;
+  int bias_mode;
 };
 
 __device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(NW * 32, (NW == 1 ? 16 : (NW == 4 ? 4 : (NW ==
     }
     __half out;
     if (PAIR) out = __float2half_rn(silu_f32(v[0]) * v[NWT - 1]);
-    else out = __float2half_rn(v[0]);
+    else out = round_out(v[0], p.bias, n0 + c, p.bias_mode);
     reinterpret_cast<__half*>(p.Y)[n0 + c] = out;
   }
 }
@@ -213,6 +215,8 @@ struct GenericArgs {
   int scales_f16[2];
   void* Y;
   int M, K, N, G, zrb, bs;
+  const __half* bias;
+  int bias_mode;
 };
 
 template <bool PAIR>
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(256) generic_kernel(const GenericArgs p) {
       if (m < p.M) {
         __half out;
         if (PAIR) out = __float2half_rn(silu_f32(acc[0][r]) * acc[NWT - 1][r]);
-        else out = __float2half_rn(acc[0][r]);
+        else out = round_out(acc[0][r], p.bias, n, p.bias_mode);
         reinterpret_cast<__half*>(p.Y)[(long long)m * p.N + n] = out;
       }
     }
@@ -364,6 +368,8 @@ cudaError_t launch_gemv_impl(LaunchCtx& ctx, const void* A, const QWeight* w, in
   a.G = K / bs;
   a.zrb = (a.G + 1) / 2;
   a.group_shift = bs >= 32 ? log2_int(bs / 32) : 0;
+  a.bias = static_cast<const __half*>(ctx.bias);
+  a.bias_mode = PAIR ? 0 : ctx.bias_mode;
   long long grid = (long long)ctx.num_sms * pl.ctas_per_sm;
   if (grid > N) grid = N;
   const long long min_grid = (N + kMaxColsPerCta - 1) / kMaxColsPerCta;
@@ -393,6 +399,8 @@ cudaError_t launch_generic_impl(LaunchCtx& ctx, const void* A, int M, const QWei
   a.G = K / bs;
   a.zrb = (a.G + 1) / 2;
   a.bs = bs;
+  a.bias = static_cast<const __half*>(ctx.bias);
+  a.bias_mode = PAIR ? 0 : ctx.bias_mode;
   dim3 grid((N + 7) / 8, (M + 7) / 8);
   ctx.variant = PAIR ? "generic_pair_swiglu" : "generic";
   return launch_kernel(ctx, generic_kernel<PAIR>, grid, dim3(256), 0, a);

@@ -44,6 +44,8 @@ struct TmaGemvArgs {
   int stage_bytes;
   int stages;
   uint32_t* status;
+  const __half* bias;
+  int bias_mode;
 };
 
 __device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
@@ -258,9 +260,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
       for (int w = 0; w < WG; ++w) s += red[w][t][c];
       v[t] = s;
     }
-    float o = PAIR ? silu_f32(v[0]) * v[NWT - 1] : v[0];
-    if (bad) o = __int_as_float(0x7fc00000);
-    reinterpret_cast<__half*>(p.Y)[n0 + c] = __float2half_rn(o);
+    __half out;
+    if (PAIR) out = __float2half_rn(silu_f32(v[0]) * v[NWT - 1]);
+    else out = round_out(v[0], p.bias, n0 + c, p.bias_mode);
+    if (bad) out = __ushort_as_half(0x7e00);
+    reinterpret_cast<__half*>(p.Y)[n0 + c] = out;
   }
 }
 
@@ -343,6 +347,8 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   a.stages = kRingBudget / a.stage_bytes;
   if (a.stages > kMaxStages) a.stages = kMaxStages;
   a.status = ctx.status;
+  a.bias = static_cast<const __half*>(ctx.bias);
+  a.bias_mode = PAIR ? 0 : ctx.bias_mode;
   int grid = ctx.num_sms;
   if (grid > N) grid = N;
   const int min_grid = (N + kMaxColsPerCta - 1) / kMaxColsPerCta;

@@ -103,6 +103,16 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t w, uint32_t a, float acc)
   return acc;
 }
 
+// Output rounding with the optional bias epilogue (matmul_nbits.rs, fold_bias_f16):
+// mode 0: fp16(acc); 1: fp16(acc + b) (bias added in fp32, one rounding);
+// 2: fp16(fp16(acc) + b) (the accumulator rounded first, as a separate add would).
+__device__ __forceinline__ __half round_out(float acc, const __half* bias, int n, int mode) {
+  if (mode == 0) return __float2half_rn(acc);
+  const float b = __half2float(bias[n]);
+  if (mode == 1) return __float2half_rn(acc + b);
+  return __float2half_rn(__half2float(__float2half_rn(acc)) + b);
+}
+
 __device__ __forceinline__ float half_bits_to_float(uint32_t h) {
   return __half2float(__ushort_as_half((unsigned short)h));
 }

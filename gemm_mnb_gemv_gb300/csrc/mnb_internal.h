@@ -19,6 +19,8 @@ struct LaunchCtx {
   bool pdl;         // launch with programmatic stream serialisation
   int num_sms;
   uint32_t* status = nullptr;     // device status word for bounded waits
+  const void* bias = nullptr;     // fp16 [N] or null
+  int bias_mode = 0;              // 0 none, 1 fp16(acc + b), 2 fp16(fp16(acc) + b)
   const char* variant = nullptr;  // set by the launcher that ran
 };
 

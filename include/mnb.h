@@ -135,6 +135,25 @@ MNB_API mnb_status mnb_gemm(const void *A, int M, mnb_weight w, const uint8_t *r
                     int block_size, void *workspace, size_t ws_bytes, void *Y,
                     mnb_stream stream);
 
+/* Bias epilogue modes for mnb_gemm_bias. */
+typedef enum {
+    MNB_BIAS_NONE = 0,         /* Y = fp16(acc)                                          */
+    MNB_BIAS_FUSED = 1,        /* Y = fp16(acc + b), one rounding (a fused MatMul+bias)   */
+    MNB_BIAS_AFTER_ROUND = 2   /* Y = fp16(fp16(acc) + b), bit-identical to mnb_gemm
+                                  followed by a separate fp16 add                          */
+} mnb_bias_mode;
+
+/*
+ * mnb_gemm with a bias [N] (fp16, one value per output column) added in the epilogue,
+ * in either of the two rounding orders of the pages' fp16 bias epilogue (matmul_nbits.rs,
+ * fold_bias_f16; marlin_gemm.rs, fold_bias): MNB_BIAS_FUSED adds b to the fp32
+ * accumulator and rounds once, MNB_BIAS_AFTER_ROUND rounds the accumulator to fp16 first
+ * and then rounds fp32(that) + b. `bias` may be NULL only with MNB_BIAS_NONE.
+ */
+MNB_API mnb_status mnb_gemm_bias(const void *A, int M, mnb_weight w, const uint8_t *repacked, int K,
+                                 int N, int block_size, const void *bias, int bias_mode,
+                                 void *workspace, size_t ws_bytes, void *Y, mnb_stream stream);
+
 /*
  * Paired gate/up projection with the SwiGLU epilogue (matmul_nbits.rs,
  * matmul_nbits_gemv_f16_gate_up_swiglu): g = A . gate^T, u = A . up^T (both M = 1,

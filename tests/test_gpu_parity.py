@@ -381,3 +381,76 @@ def test_gate_up_swiglu_weights_with_different_storage(env):
     tol = orc.swiglu_tolerance(g, bg, u, bu, ref)
     got = out.cpu().numpy().astype(np.float64)[None, :]
     assert np.all(np.abs(got - ref) <= tol)
+
+
+def test_mlp_chain_gate_up_then_down_full_size(env):
+    """Decode MLP: the SwiGLU output (fp16, on the device) feeds the down GEMV directly,
+    launched back to back with programmatic dependent launch.  Each step is checked
+    against the oracle on the input it actually received."""
+    mnb, torch, dev = env
+    wgl = syn.WORKLOADS["mlp_gate_up_k4096_n14336"]
+    wdl = syn.WORKLOADS["mlp_down_k14336_n4096"]
+    wg, wu, wd = syn.make_weight(wgl, "gate"), syn.make_weight(wgl, "up"), syn.make_weight(wdl, "B")
+    A = syn.make_activation(wgl)
+    tg, tu, td = upload_weight(wg, dev), upload_weight(wu, dev), upload_weight(wd, dev)
+    x = upload_act(A.reshape(-1), dev)
+    mnb.mnb_set_programmatic_launch(True)
+    try:
+        h = mnb.mnb_gemv_gate_up_swiglu(x, tg, tu, wgl.K, wgl.N, wgl.block_size)
+        y = mnb.mnb_gemv(h, *td, wdl.K, wdl.N, wdl.block_size)
+    finally:
+        mnb.mnb_set_programmatic_launch(False)
+    torch.cuda.synchronize()
+    ref, g, bg, u, bu = orc.gate_up_swiglu(A, (wg.packed, wg.scales, wg.zero_points),
+                                           (wu.packed, wu.scales, wu.zero_points), wgl.K, wgl.N, wgl.block_size)
+    hh = h.cpu().numpy()
+    assert np.all(np.abs(hh.astype(np.float64)[None, :] - ref) <= orc.swiglu_tolerance(g, bg, u, bu, ref))
+    Y, B = orc.matmul(hh[None, :], wd.packed, wd.scales, wd.zero_points, wdl.K, wdl.N, wdl.block_size)
+    assert_within_bound(y.cpu().numpy()[None, :], Y, B, "down after swiglu")
+
+
+BIAS_CASES = [  # (M, K, N, bs, expected variant prefix)
+    (1, 4096, 4096, 32, "gemv_tma_ring"),
+    (1, 96, 130, 32, "gemv_f16acc32"),
+    (1, 48, 33, 16, "generic"),
+    (4, 4096, 300, 64, "gemm_smallm"),
+    (3, 96, 77, 16, "generic"),
+    (64, 256, 300, 128, "gemm_tcgen05"),
+]
+
+
+@pytest.mark.parametrize("M,K,N,bs,variant", BIAS_CASES)
+def test_bias_epilogue_both_rounding_modes(env, M, K, N, bs, variant):
+    """Mode 2 (round, then add) is bit-identical to mnb_gemm followed by a plain fp16 add;
+    mode 1 (add, then round once) is within the product bound plus one fp16 rounding."""
+    mnb, torch, dev = env
+    wl = syn.custom(f"bias_{M}_{K}_{N}_{bs}", M, K, N, bs)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    bias_np = (syn.normal(syn.fnv1a64(f"{wl.name}/bias"), N) * 2.0).astype(np.float16)
+    packed, scales, zpt = upload_weight(w, dev)
+    a = upload_act(A, dev)
+    rp = mnb.mnb_repack(packed, K, N, bs) if M > 16 else None
+    bias = torch.from_numpy(bias_np).to(dev)
+    y0 = mnb.mnb_gemm(a, packed, scales, zpt, K, N, bs, repacked=rp)
+    y2 = mnb.mnb_gemm_bias(a, packed, scales, zpt, K, N, bs, bias, mnb.MNB_BIAS_AFTER_ROUND, repacked=rp)
+    assert mnb.mnb_last_variant().startswith(variant)
+    y1 = mnb.mnb_gemm_bias(a, packed, scales, zpt, K, N, bs, bias, mnb.MNB_BIAS_FUSED, repacked=rp)
+    torch.cuda.synchronize()
+    two_op = (y0.float() + bias.float()[None, :]).half()
+    assert torch.equal(y2.view(torch.int16), two_op.view(torch.int16))
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
+    ref = Y + orc.f16_to_f64(bias_np)[None, :]
+    got = y1.cpu().numpy().astype(np.float64)
+    tol = 2e-3 * B + 2.0 ** -11 * np.abs(ref) + 1e-5
+    assert np.all(np.abs(got - ref) <= tol)
+
+
+def test_bias_mode_validation(env):
+    mnb, torch, dev = env
+    a = torch.zeros(64, dtype=torch.float16, device=dev)
+    packed = torch.zeros((8, 32), dtype=torch.uint8, device=dev)
+    scales = torch.ones((8, 2), dtype=torch.float16, device=dev)
+    with pytest.raises(mnb.MnbError) as e:
+        mnb.mnb_gemm_bias(a, packed, scales, None, 64, 8, 32, torch.zeros(8, dtype=torch.float16, device=dev), 5)
+    assert e.value.status == mnb.MNB_ERR_INVALID_ARG
