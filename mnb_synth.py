@@ -135,6 +135,30 @@ def make_weight(wl: Workload, tag: str = "B") -> QuantWeight:
     return QuantWeight(packed=packed, scales=scales, zero_points=zp)
 
 
+def make_g_idx(wl: Workload, kind: str = "act_order", tag: str = "g_idx") -> np.ndarray:
+    """int32 ``[K]`` group indices, the optional act-order input of MatMulNBits.
+
+    ``"act_order"``: the K columns are visited in a random order and each run of
+    ``block_size`` consecutive visits is one group, so every group has ``block_size``
+    members scattered over K (the structure act-order quantisation produces).
+    ``"uneven"``: every k draws a uniform random group, so group sizes vary and some
+    groups may be empty.  ``"identity"``: group ``k // block_size``, the plain layout.
+    """
+    seed = fnv1a64(f"{wl.name}/{tag}")
+    G = wl.k_blocks
+    if kind == "act_order":
+        visit = np.argsort(uniform01(seed, wl.K), kind="stable")
+        g = np.empty(wl.K, dtype=np.int64)
+        g[visit] = np.arange(wl.K) // wl.block_size
+    elif kind == "uneven":
+        g = np.minimum((uniform01(seed, wl.K) * G).astype(np.int64), G - 1)
+    elif kind == "identity":
+        g = np.arange(wl.K) // wl.block_size
+    else:
+        raise ValueError(kind)
+    return g.astype(np.int32)
+
+
 # The five problem families this library is measured on.  Names say what they are.
 WORKLOADS = {
     "tiny_gemv_k256_n128": Workload("tiny_gemv_k256_n128", 1, 256, 128, 32, "f16", 0.005, 0.02, True, "uniform1"),

@@ -126,23 +126,46 @@ def scales_f64(scales: np.ndarray, K: int, N: int, block_size: int) -> np.ndarra
 # ---------------------------------------------------------------------------
 
 
-def weight_nk(packed, scales, zp, K: int, N: int, block_size: int) -> np.ndarray:
-    """Exact fp64 ``w[n, k] = (code[n, k] - zp[n, g]) * scale[n, g]``, ``g = k // bs``."""
+def groups(K: int, block_size: int, g_idx=None) -> np.ndarray:
+    """int64 ``[K]``: the group whose scale and zero point apply at each ``k``.
+
+    Without ``g_idx`` it is the block ``k // bs``.  With the act-order input ``g_idx``
+    (int32 ``[K]`` or ``[k_blocks * bs]``; entries past ``K`` are never read) it is
+    ``g_idx[k]`` (``matmul_nbits_dequant_f32``: ``group = group_indices[depth]``).  The
+    code itself is always read from block ``k // bs``.
+    """
+    if g_idx is None:
+        return np.arange(K, dtype=np.int64) // block_size
+    g = np.asarray(g_idx).reshape(-1).astype(np.int64)
+    if g.size not in (K, k_blocks(K, block_size) * block_size):
+        raise ValueError(f"g_idx has {g.size} entries, expected {K} or the padded K")
+    return g[:K]
+
+
+def weight_nk(packed, scales, zp, K: int, N: int, block_size: int, g_idx=None) -> np.ndarray:
+    """Exact fp64 ``w[n, k] = (code[n, k] - zp[n, g]) * scale[n, g]``, ``g = groups(k)``.
+
+    A group outside ``0 .. k_blocks-1`` gives ``w = 0`` (``matmul_nbits_dequant_f32``
+    writes 0 for it; the operator's host check rejects such a ``g_idx`` outright).
+    """
     c = codes(packed, K, N, block_size)
     z = zero_points(zp, K, N, block_size)
     s = scales_f64(scales, K, N, block_size)
-    g = np.arange(K) // block_size
-    return (c - z[:, g]).astype(np.float64) * s[:, g]
+    g = groups(K, block_size, g_idx)
+    ok = (g >= 0) & (g < k_blocks(K, block_size))
+    gc = np.where(ok, g, 0)
+    w = (c - z[:, gc]).astype(np.float64) * s[:, gc]
+    return np.where(ok[None, :], w, 0.0)
 
 
-def dequant_kn_f32(packed, scales, zp, K: int, N: int, block_size: int) -> np.ndarray:
+def dequant_kn_f32(packed, scales, zp, K: int, N: int, block_size: int, g_idx=None) -> np.ndarray:
     """fp32 ``[K, N]``: each element is ``(code - zp) * scale`` rounded once to fp32.
 
     ``matmul_nbits_dequant_f32`` writes this matrix at ``depth * N + n``.  The fp64
     product is exact, so one rounding gives the correctly rounded fp32 product; for
     fp16 scales the product is already representable in fp32 and the value is exact.
     """
-    return weight_nk(packed, scales, zp, K, N, block_size).T.astype(np.float32)
+    return weight_nk(packed, scales, zp, K, N, block_size, g_idx).T.astype(np.float32)
 
 
 def activations_f64(A: np.ndarray) -> np.ndarray:
@@ -151,18 +174,19 @@ def activations_f64(A: np.ndarray) -> np.ndarray:
     return f16_to_f64(A).reshape(A.shape)
 
 
-def matmul(A, packed, scales, zp, K: int, N: int, block_size: int):
+def matmul(A, packed, scales, zp, K: int, N: int, block_size: int, g_idx=None):
     """``(Y, B)``: fp64 ``Y = A . w^T`` and the bound ``B = |A| . |w|^T``, both ``[M, N]``.
 
     ``A`` is the fp16 activation ``[M, K]`` (taken at its fp16 value, as the pages'
-    oracles consume the same fp16-rounded activations as the kernel).
+    oracles consume the same fp16-rounded activations as the kernel).  ``g_idx``: see
+    ``groups``.
     """
     a = activations_f64(A).reshape(-1, K)
-    w = weight_nk(packed, scales, zp, K, N, block_size)
+    w = weight_nk(packed, scales, zp, K, N, block_size, g_idx)
     return a @ w.T, np.abs(a) @ np.abs(w).T
 
 
-def matmul_rows(A, packed, scales, zp, K: int, N: int, block_size: int, rows, cols):
+def matmul_rows(A, packed, scales, zp, K: int, N: int, block_size: int, rows, cols, g_idx=None):
     """``(Y, B)`` at the listed ``(row, col)`` pairs only (full-size spot checks)."""
     rows = np.asarray(rows, dtype=np.int64)
     cols = np.asarray(cols, dtype=np.int64)
@@ -173,7 +197,7 @@ def matmul_rows(A, packed, scales, zp, K: int, N: int, block_size: int, rows, co
     sub_packed = np.ascontiguousarray(packed).reshape(N, G * blob)[ucols]
     sub_scales = np.ascontiguousarray(scales).reshape(N, G)[ucols]
     sub_zp = None if zp is None else np.ascontiguousarray(zp).reshape(N, -1)[ucols]
-    w = weight_nk(sub_packed, sub_scales, sub_zp, K, len(ucols), block_size)
+    w = weight_nk(sub_packed, sub_scales, sub_zp, K, len(ucols), block_size, g_idx)
     ar = a[rows]
     wc = w[inv]
     return np.einsum("ik,ik->i", ar, wc), np.einsum("ik,ik->i", np.abs(ar), np.abs(wc))
@@ -270,3 +294,83 @@ def unrepack_codes(repacked: np.ndarray, K: int, N: int) -> np.ndarray:
     byte, half = _repack_positions(K, N)
     v = np.asarray(repacked).reshape(-1)[byte].astype(np.int64)
     return np.where(half == 1, v >> 4, v & 15)
+
+
+# ---------------------------------------------------------------------------
+# Act-order weights prepared for the block kernels
+# ---------------------------------------------------------------------------
+#
+# With ``g_idx`` the members of a group are scattered over K.  Reordering k so that
+# each group's members sit together turns the weight into a plain block weight:
+#
+#   * groups in ascending order; inside a group, its members in ascending k;
+#   * each group's run padded with empty slots (-1) to a whole number of blocks;
+#   * ``perm[k']`` = the source k of prepared position k' (or -1), ``K' = len(perm)``,
+#     ``block_group[j]`` = the group of prepared block j.
+#
+# The prepared weight has codes ``code[n, perm[k']]`` (the block's zero point at an
+# empty slot, so its weight is 0), and the scale and zero point of ``block_group[j]``
+# for block j.  The matching activation is ``A'[m, k'] = A[m, perm[k']]`` (0 at an
+# empty slot), and ``A' . w'^T = A . w^T`` term by term.  This preparation is this
+# library's own; the pages dequantise with ``g_idx`` directly.
+
+
+def act_order_plan(g_idx, K: int, block_size: int):
+    """``(K_prepared, perm, block_group)`` for a valid ``g_idx`` (int32 arrays).
+
+    Raises ``ValueError`` for an entry outside ``0 .. k_blocks-1`` (the operator's own
+    check on ``g_idx``, matmul_nbits.rs).
+    """
+    G = k_blocks(K, block_size)
+    g = groups(K, block_size, g_idx)
+    bad = np.nonzero((g < 0) | (g >= G))[0]
+    if bad.size:
+        raise ValueError(f"g_idx[{bad[0]}]={g[bad[0]]} is outside 0..{G}")
+    perm, block_group = [], []
+    for grp in range(G):
+        members = np.nonzero(g == grp)[0].tolist()
+        nblocks = -(-len(members) // block_size)
+        perm += members + [-1] * (nblocks * block_size - len(members))
+        block_group += [grp] * nblocks
+    return len(perm), np.array(perm, dtype=np.int32), np.array(block_group, dtype=np.int32)
+
+
+def _pack_nibbles(v: np.ndarray) -> np.ndarray:
+    """uint8 rows from int rows of 4-bit values: low nibble from the even position."""
+    v = np.asarray(v, dtype=np.int64)
+    if v.shape[1] % 2:
+        v = np.concatenate([v, np.zeros((v.shape[0], 1), dtype=np.int64)], axis=1)
+    return (v[:, 0::2] | (v[:, 1::2] << 4)).astype(np.uint8)
+
+
+def act_order_prepare(packed, scales, zp, K: int, N: int, block_size: int, perm, block_group):
+    """``(packed', scales', zero_points')`` of the prepared ``K' x N`` block weight.
+
+    ``packed'`` is uint8 ``[N, K'/2]``, ``scales'`` keeps the scale dtype
+    ``[N, K'/bs]``, ``zero_points'`` is uint8 ``[N, ceil(K'/bs/2)]`` (the unused high
+    nibble of an odd count is 0), or ``None`` when the weight has none.
+    """
+    perm = np.asarray(perm, dtype=np.int64)
+    bg = np.asarray(block_group, dtype=np.int64)
+    Kp = perm.size
+    if Kp % block_size or bg.size != Kp // block_size:
+        raise ValueError("perm and block_group do not describe whole blocks")
+    c = codes(packed, K, N, block_size)
+    z = zero_points(zp, K, N, block_size)
+    zb = z[:, bg]                                         # [N, K'/bs]
+    zk = zb[:, np.arange(Kp) // block_size]               # [N, K']
+    cp = np.where(perm[None, :] >= 0, c[:, np.maximum(perm, 0)], zk)
+    G = k_blocks(K, block_size)
+    sp = np.ascontiguousarray(scales).reshape(N, G)[:, bg].copy()
+    zpp = None if zp is None else _pack_nibbles(zb)
+    return _pack_nibbles(cp), sp, zpp
+
+
+def act_order_gather(A, perm) -> np.ndarray:
+    """fp16 ``A'[m, k'] = A[m, perm[k']]``, and +0 where ``perm[k'] = -1``."""
+    A = np.asarray(A)
+    perm = np.asarray(perm, dtype=np.int64)
+    out = np.zeros((A.shape[0], perm.size), dtype=A.dtype)
+    ok = perm >= 0
+    out[:, ok] = A[:, perm[ok]]
+    return out

@@ -9,7 +9,11 @@
   the default zero point 8 equals an explicit 0x88 buffer,
 * fp16 decoding against numpy's own conversion for all 65536 bit patterns,
 * silu against ``x * scipy.special.expit(x)``,
-* the repacked layout: a hand-placed code, and the round trip.
+* the repacked layout: a hand-placed code, and the round trip,
+* act-order ``g_idx``: the identity reduces to the plain layout; a weight built the
+  act-order way (codes quantised in a visit order, stored in k order) dequantises to
+  the same matrix; exact rational brute force with uneven and out-of-range groups;
+  a hand-worked preparation plan; the prepared weight holds the same weights.
 """
 from __future__ import annotations
 
@@ -300,3 +304,136 @@ def test_synth_streams_are_deterministic():
     # SplitMix64 reference outputs for seed 0 (first three values of the published generator)
     z = syn.splitmix64(0, 3)
     assert [int(x) for x in z] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+# ---------------------------------------------------------------------------
+# Act-order g_idx (matmul_nbits.rs, matmul_nbits_dequant_f32 and the g_idx check)
+# ---------------------------------------------------------------------------
+
+
+def test_g_idx_identity_equals_plain_layout():
+    wl = syn.custom("pin_gidx_identity", 2, 256, 9, 32)
+    w = syn.make_weight(wl)
+    g_idx = np.repeat(np.arange(wl.k_blocks, dtype=np.int32), wl.block_size)
+    plain = orc.weight_nk(w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size)
+    act = orc.weight_nk(w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size, g_idx)
+    np.testing.assert_array_equal(act, plain)
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64])
+def test_g_idx_act_order_construction(bs):
+    """Quantise in a visit order v (group = step // bs), store codes in k order: the
+    g_idx weight at column v[j] equals the plain weight of the visit-ordered codes at j."""
+    K, N = 8 * bs, 5
+    G = K // bs
+    rng = np.random.default_rng(bs)
+    q = rng.integers(0, 16, size=(N, K))          # codes in visit order
+    zp = rng.integers(0, 16, size=(N, G))
+    scales = rng.uniform(0.01, 0.1, size=(N, G)).astype(np.float16)
+    v = rng.permutation(K)                         # v[j] = the k visited at step j
+    stored = np.empty_like(q)
+    stored[:, v] = q
+    g_idx = np.empty(K, dtype=np.int32)
+    g_idx[v] = np.arange(K) // bs
+    w_act = orc.weight_nk(_pack_codes(stored), scales, _pack_zp(zp), K, N, bs, g_idx)
+    w_plain = orc.weight_nk(_pack_codes(q), scales, _pack_zp(zp), K, N, bs)
+    np.testing.assert_array_equal(w_act[:, v], w_plain)
+
+
+def test_g_idx_exact_rational_brute_force():
+    """Uneven groups and two out-of-range entries (which contribute nothing)."""
+    wl = syn.custom("pin_gidx_rational", 2, 64, 3, 16, scales_dtype="f32")
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    K, N, bs, G = wl.K, wl.N, wl.block_size, wl.k_blocks
+    g_idx = syn.make_g_idx(wl, "uneven").copy()
+    g_idx[5], g_idx[40] = -1, G
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs, g_idx)
+    for m in range(wl.M):
+        for n in range(N):
+            acc = fractions.Fraction(0)
+            row = w.packed[n].tobytes()
+            for k in range(K):
+                g = int(g_idx[k])
+                if not 0 <= g < G:
+                    continue
+                b = row[k // 2]
+                code = (b >> 4) if k % 2 else (b & 15)
+                zb = int(w.zero_points[n][g // 2])
+                zpv = (zb >> 4) if g % 2 else (zb & 15)
+                s = fractions.Fraction(float(w.scales[n, g]))
+                acc += fractions.Fraction(float(A[m, k])) * (code - zpv) * s
+            assert abs(Y[m, n] - float(acc)) <= 1e-12 * max(1.0, B[m, n])
+
+
+def test_act_order_plan_hand_worked():
+    """K = 12, bs = 4, three groups of sizes 5, 1 and 6, worked out by hand:
+    group 0 = k {1, 2, 6, 9, 10} -> 2 blocks, group 1 = {4} -> 1, group 2 =
+    {0, 3, 5, 7, 8, 11} -> 2; empty slots close each group's last block."""
+    g_idx = np.array([2, 0, 0, 2, 1, 2, 0, 2, 2, 0, 0, 2], dtype=np.int32)
+    Kp, perm, bg = orc.act_order_plan(g_idx, 12, 4)
+    assert Kp == 20
+    assert perm.tolist() == [1, 2, 6, 9, 10, -1, -1, -1, 4, -1, -1, -1,
+                             0, 3, 5, 7, 8, 11, -1, -1]
+    assert bg.tolist() == [0, 0, 1, 2, 2]
+
+
+def test_act_order_plan_balanced_keeps_k():
+    wl = syn.custom("pin_plan_balanced", 1, 1024, 4, 128)
+    g_idx = syn.make_g_idx(wl, "act_order")
+    Kp, perm, bg = orc.act_order_plan(g_idx, wl.K, wl.block_size)
+    assert Kp == wl.K
+    assert sorted(perm.tolist()) == list(range(wl.K))
+    np.testing.assert_array_equal(g_idx[perm], np.arange(wl.K) // wl.block_size)
+    assert bg.tolist() == list(range(wl.k_blocks))
+
+
+def test_act_order_plan_rejects_out_of_range():
+    g_idx = np.zeros(64, dtype=np.int32)
+    g_idx[7] = 4
+    with pytest.raises(ValueError, match=r"g_idx\[7\]=4"):
+        orc.act_order_plan(g_idx, 64, 16)
+    g_idx[7] = -1
+    with pytest.raises(ValueError):
+        orc.act_order_plan(g_idx, 64, 16)
+
+
+@pytest.mark.parametrize("kind,has_zp,sdt", [("act_order", True, "f16"), ("uneven", True, "f32"),
+                                              ("uneven", False, "f16"), ("identity", True, "f16")])
+def test_act_order_prepare_holds_the_same_weights(kind, has_zp, sdt):
+    wl = syn.custom(f"pin_prepare_{kind}_{has_zp}_{sdt}", 1, 512, 7, 32, scales_dtype=sdt, has_zp=has_zp)
+    w = syn.make_weight(wl)
+    g_idx = syn.make_g_idx(wl, kind)
+    Kp, perm, bg = orc.act_order_plan(g_idx, wl.K, wl.block_size)
+    pk, sc, zp = orc.act_order_prepare(w.packed, w.scales, w.zero_points, wl.K, wl.N,
+                                       wl.block_size, perm, bg)
+    assert pk.shape == (wl.N, Kp // 2) and sc.shape == (wl.N, Kp // wl.block_size)
+    assert sc.dtype == w.scales.dtype and (zp is None) == (not has_zp)
+    w_prep = orc.weight_nk(pk, sc, zp, Kp, wl.N, wl.block_size)
+    w_orig = orc.weight_nk(w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size, g_idx)
+    real = perm >= 0
+    np.testing.assert_array_equal(w_prep[:, real], w_orig[:, perm[real]])
+    np.testing.assert_array_equal(w_prep[:, ~real], 0.0)
+    if kind == "identity":
+        assert Kp == wl.K and perm.tolist() == list(range(wl.K))
+        np.testing.assert_array_equal(pk, w.packed)
+
+
+def test_act_order_product_equivalence_exact():
+    """Integer activations and power-of-two scales: every sum is exact in fp64, so the
+    gathered product over the prepared weight equals the g_idx product bit for bit."""
+    K, N, M, bs = 256, 6, 3, 32
+    G = K // bs
+    rng = np.random.default_rng(5)
+    packed = rng.integers(0, 256, size=(N, K // 2)).astype(np.uint8)
+    zp = rng.integers(0, 256, size=(N, -(-G // 2))).astype(np.uint8)
+    scales = (2.0 ** rng.integers(-6, 0, size=(N, G))).astype(np.float16)
+    A = rng.integers(-9, 10, size=(M, K)).astype(np.float16)
+    g_idx = rng.integers(0, G, size=K).astype(np.int32)
+    Y, _ = orc.matmul(A, packed, scales, zp, K, N, bs, g_idx)
+    Kp, perm, bg = orc.act_order_plan(g_idx, K, bs)
+    pk, sc, zpp = orc.act_order_prepare(packed, scales, zp, K, N, bs, perm, bg)
+    Ag = orc.act_order_gather(A, perm)
+    Y2, _ = orc.matmul(Ag, pk, sc, zpp, Kp, N, bs)
+    np.testing.assert_array_equal(Y2, Y)
+    assert np.all(Ag[:, perm < 0] == 0) and not np.any(np.signbit(Ag[:, perm < 0]))
