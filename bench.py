@@ -268,6 +268,35 @@ class DeviceBench:
         return {"workload": "mlp_chain_gate_up_k4096_n14336_down", "us_per_call": us,
                 "gbps": nbytes / (us * 1e3), "copies": ncopy, "variant": "gate_up_swiglu + down gemv"}
 
+    def act_order(self, wl, steps, warmup, sampler, calls=200, kind="act_order"):
+        """M-row product of an act-order weight: the activation gather and the block kernel
+        on the prepared weight, per call (two launches)."""
+        torch, mnb = self.torch, self.mnb
+        g_idx = syn.make_g_idx(wl, kind)
+        kp, perm, bg = mnb.mnb_act_order_plan(g_idx, wl.K, wl.block_size)
+        perm_d = torch.from_numpy(perm).to(self.dev)
+        bg_d = torch.from_numpy(bg).to(self.dev)
+        wlp = syn.custom(wl.name + "_prepared", wl.M, kp, wl.N, wl.block_size, wl.scales_dtype, wl.has_zp)
+        ncopy = self.copies_for(weight_bytes(wlp))
+        w, raw = self.upload_weights(wl, "B", 1)
+        base = mnb.mnb_act_order_prepare(*raw[0], wl.K, wl.N, wl.block_size, perm_d, bg_d, kp)
+        del raw
+        copies = [base] + [tuple(None if x is None else x.clone() for x in base) for _ in range(ncopy - 1)]
+        A = torch.from_numpy(syn.make_activation(wl)).to(self.dev)
+        Y = torch.empty((wl.M, wl.N), dtype=torch.float16, device=self.dev)
+        ws = torch.empty(mnb.mnb_act_order_workspace_bytes(wl.M, kp), dtype=torch.uint8, device=self.dev)
+
+        def rec():
+            for i in range(calls):
+                mnb.mnb_gemm_act_order(A, *copies[i % ncopy], perm_d, wl.K, kp, wl.N, wl.block_size,
+                                       workspace=ws, out=Y)
+
+        ms, _ = self.time_graph(rec, 2 * calls, steps, warmup, sampler)
+        us = ms * 1e3 / calls
+        return {"workload": f"{wl.name}_{kind}", "K_prepared": kp, "us_per_call": us,
+                "gbps": call_bytes(wl) / (us * 1e3), "copies": ncopy,
+                "variant": "act_order_gather + " + mnb.mnb_last_variant()}
+
     def gemm(self, wl, steps, warmup, sampler, calls, repacked: bool):
         torch, mnb = self.torch, self.mnb
         per_copy = weight_bytes(wl) + wl.M * wl.K * 2
@@ -426,6 +455,8 @@ def run_single(db, name, steps, warmup):
         return db.gemm(W[f"{name}_k4096_n4096"], steps, warmup, None, calls=200, repacked=False)
     if name == "mlp_chain":
         return db.mlp_chain(steps, warmup, None)
+    if name == "act_order_attn":
+        return db.act_order(W[HEADLINE], steps, warmup, None)
     if name == "prefill":
         return db.gemm(W["prefill_m2048_k4096_n14336"], steps, warmup, None, calls=9, repacked=True)
     raise SystemExit(f"unknown workload {name}")
@@ -441,7 +472,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, short CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
-                    help="time one workload only (attn, gate_up, down, verify_m2/4/8/16, prefill) "
+                    help="time one workload only (attn, gate_up, down, verify_m2/4/8/16, prefill, mlp_chain, "
+                         "act_order_attn) "
                          "and print its record; for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -496,6 +528,7 @@ def main():
         extras["prefill"] = db.gemm(syn.WORKLOADS["prefill_m2048_k4096_n14336"], 10, 3, sampler,
                                     calls=9, repacked=True)
         extras["mlp_chain"] = db.mlp_chain(10, 3, sampler)
+        extras["act_order_attn"] = db.act_order(wl, 20, 3, sampler)
     for k, v in extras.items():
         log(f"{k}: {v['us_per_call']:.3f} us/call, {v.get('gbps', 0):.1f} GB/s, "
             f"{v.get('tflops', 0):.1f} TFLOP/s ({v['variant']})")
@@ -528,7 +561,6 @@ def main():
                           "frac": pf["tflops"] / tc,
                           "peak_source": f"{peak_src} bf16_tflops (burst; fp16 rate equals bf16)"}
         for k, v in extras.items():
-            wlx = syn.WORKLOADS[v["workload"]]
             if "gbps" in v and k != "prefill":
                 v["hbm_frac"] = v["gbps"] / hbm
         line["secondary"] = extras

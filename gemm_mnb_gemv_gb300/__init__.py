@@ -8,7 +8,9 @@ output tensor is not passed, the binding allocates it with torch before the call
 
 The names match the C entry points: ``mnb_dequant``, ``mnb_repacked_bytes``,
 ``mnb_repack``, ``mnb_gemv``, ``mnb_workspace_bytes``, ``mnb_gemm``,
-``mnb_gemm_bias``, ``mnb_gemv_gate_up_swiglu``, ``mnb_set_programmatic_launch``,
+``mnb_gemm_bias``, ``mnb_gemv_gate_up_swiglu``, ``mnb_dequant_gidx``,
+``mnb_act_order_plan``, ``mnb_act_order_prepare``, ``mnb_act_order_gather``,
+``mnb_act_order_workspace_bytes``, ``mnb_gemm_act_order``, ``mnb_set_programmatic_launch``,
 ``mnb_check_device_status``,
 ``mnb_last_error``,
 ``mnb_last_variant``, ``mnb_version``.
@@ -62,6 +64,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mnb_gemm": (c_int, [vp, c_int, MnbWeight, vp, c_int, c_int, c_int, vp, c_size, vp, vp]),
         "mnb_gemv_gate_up_swiglu": (c_int, [vp, MnbWeight, MnbWeight, c_int, c_int, c_int, vp, vp]),
         "mnb_gemm_bias": (c_int, [vp, c_int, MnbWeight, vp, c_int, c_int, c_int, vp, c_int, vp, c_size, vp, vp]),
+        "mnb_dequant_gidx": (c_int, [MnbWeight, vp, c_int, c_int, c_int, vp, vp]),
+        "mnb_act_order_plan": (c_int, [vp, c_int, c_int, vp, vp, vp]),
+        "mnb_act_order_prepare": (c_int, [MnbWeight, c_int, c_int, c_int, vp, vp, c_int, vp, vp, vp, vp]),
+        "mnb_act_order_gather": (c_int, [vp, c_int, c_int, vp, c_int, vp, vp]),
+        "mnb_act_order_workspace_bytes": (c_size, [c_int, c_int]),
+        "mnb_gemm_act_order": (c_int, [vp, c_int, MnbWeight, vp, vp, c_int, c_int, c_int, c_int, vp, c_int, vp,
+                                       c_size, vp, vp]),
         "mnb_set_programmatic_launch": (None, [c_int]),
         "mnb_check_device_status": (c_int, []),
         "mnb_last_error": (ctypes.c_char_p, []),
@@ -250,4 +259,109 @@ def mnb_gemv_gate_up_swiglu(A, gate, up, K: int, N: int, block_size: int, out=No
     _check_dev("out", out, torch.float16)
     _raise(lib.mnb_gemv_gate_up_swiglu(_ptr(A), wg, wu, K, N, block_size, _ptr(out),
                                        _stream_handle(stream)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Act-order (g_idx) weights
+# ---------------------------------------------------------------------------
+
+
+def mnb_dequant_gidx(packed, scales, zero_points, g_idx, K: int, N: int, block_size: int, out=None,
+                     stream=None):
+    """fp32 ``[K, N]`` with the scale and zero point of group ``g_idx[k]`` at column ``k``."""
+    torch = _torch()
+    lib = load_library()
+    w = _weight(packed, scales, zero_points)
+    _check_dev("g_idx", g_idx, torch.int32)
+    if out is None:
+        out = torch.empty((K, N), dtype=torch.float32, device=packed.device)
+    _check_dev("out", out, torch.float32)
+    _raise(lib.mnb_dequant_gidx(w, _ptr(g_idx), K, N, block_size, _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def mnb_act_order_plan(g_idx, K: int, block_size: int):
+    """Host-only: ``(K_prepared, perm, block_group)`` as int / int32 numpy arrays.
+
+    ``g_idx`` is any host int sequence of length ``K`` (numpy array, list or CPU tensor).
+    """
+    import numpy as np
+    lib = load_library()
+    g = np.ascontiguousarray(np.asarray(g_idx), dtype=np.int32).reshape(-1)
+    if g.size != K:
+        raise MnbError(MNB_ERR_INVALID_ARG, f"mnb_act_order_plan: g_idx has {g.size} entries, expected {K}")
+    kp = ctypes.c_int32(0)
+    gp = g.ctypes.data_as(ctypes.c_void_p)
+    _raise(lib.mnb_act_order_plan(gp, K, block_size, ctypes.byref(kp), None, None))
+    perm = np.empty(max(kp.value, 1), dtype=np.int32)
+    bg = np.empty(max(kp.value // block_size, 1), dtype=np.int32)
+    _raise(lib.mnb_act_order_plan(gp, K, block_size, ctypes.byref(kp), perm.ctypes.data_as(ctypes.c_void_p),
+                                  bg.ctypes.data_as(ctypes.c_void_p)))
+    return kp.value, perm[:kp.value], bg[:kp.value // block_size]
+
+
+def mnb_act_order_prepare(packed, scales, zero_points, K: int, N: int, block_size: int, perm, block_group,
+                          K_prepared: int, packed_out=None, scales_out=None, zero_points_out=None, stream=None):
+    """Prepared block weight ``(packed', scales', zero_points')`` (device tensors)."""
+    torch = _torch()
+    lib = load_library()
+    w = _weight(packed, scales, zero_points)
+    _check_dev("perm", perm, torch.int32)
+    _check_dev("block_group", block_group, torch.int32)
+    Gp = K_prepared // block_size
+    dev = packed.device
+    if packed_out is None:
+        packed_out = torch.empty((N, K_prepared // 2), dtype=torch.uint8, device=dev)
+    if scales_out is None:
+        scales_out = torch.empty((N, Gp), dtype=scales.dtype, device=dev)
+    if zero_points is not None and zero_points_out is None:
+        zero_points_out = torch.empty((N, (Gp + 1) // 2), dtype=torch.uint8, device=dev)
+    if zero_points is None:
+        zero_points_out = None
+    _raise(lib.mnb_act_order_prepare(w, K, N, block_size, _ptr(perm), _ptr(block_group), K_prepared,
+                                     _ptr(packed_out), _ptr(scales_out), _ptr(zero_points_out),
+                                     _stream_handle(stream)))
+    return packed_out, scales_out, zero_points_out
+
+
+def mnb_act_order_gather(A, K: int, perm, K_prepared: int, out=None, stream=None):
+    """fp16 ``[M, K']`` with ``out[m, k'] = A[m, perm[k']]`` (0 where ``perm = -1``)."""
+    torch = _torch()
+    lib = load_library()
+    _check_dev("A", A, torch.float16)
+    _check_dev("perm", perm, torch.int32)
+    M = A.numel() // K
+    if out is None:
+        out = torch.empty((M, K_prepared), dtype=torch.float16, device=A.device)
+    _check_dev("out", out, torch.float16)
+    _raise(lib.mnb_act_order_gather(_ptr(A), M, K, _ptr(perm), K_prepared, _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def mnb_act_order_workspace_bytes(M: int, K_prepared: int) -> int:
+    return int(load_library().mnb_act_order_workspace_bytes(M, K_prepared))
+
+
+def mnb_gemm_act_order(A, packed, scales, zero_points, perm, K: int, K_prepared: int, N: int, block_size: int,
+                       repacked=None, bias=None, bias_mode: int = MNB_BIAS_NONE, workspace=None, out=None,
+                       stream=None):
+    """fp16 ``[M, N]`` for an act-order weight; ``packed/scales/zero_points/repacked`` are the prepared ones."""
+    torch = _torch()
+    lib = load_library()
+    _check_dev("A", A, torch.float16)
+    _check_dev("perm", perm, torch.int32)
+    _check_dev("bias", bias, torch.float16)
+    _check_dev("repacked", repacked, torch.uint8)
+    M = A.numel() // K
+    w = _weight(packed, scales, zero_points)
+    if workspace is None:
+        workspace = torch.empty(mnb_act_order_workspace_bytes(M, K_prepared), dtype=torch.uint8, device=A.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check_dev("out", out, torch.float16)
+    _raise(lib.mnb_gemm_act_order(_ptr(A), M, w, _ptr(repacked), _ptr(perm), K, K_prepared, N, block_size,
+                                  _ptr(bias), bias_mode, _ptr(workspace), ws_bytes, _ptr(out),
+                                  _stream_handle(stream)))
     return out

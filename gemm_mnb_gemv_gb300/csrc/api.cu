@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "mnb.h"
 #include "mnb_internal.h"
@@ -141,8 +142,12 @@ mnb_status mnb_check_device_status(void) {
   const uint32_t zero = 0;
   e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero));
   if (e != cudaSuccess) return cuda_fail(fn, e);
-  return fail(MNB_ERR_TIMEOUT, "%s: a device-side wait gave up (status bits 0x%x: 1 = stage wait, "
-              "2 = slot wait, 4 = tensor-core pipeline wait); outputs of that call are NaN", fn, v);
+  if (v & 7u)
+    return fail(MNB_ERR_TIMEOUT, "%s: a device-side wait gave up (status bits 0x%x: 1 = stage wait, "
+                "2 = slot wait, 4 = tensor-core pipeline wait, 8 = index out of range); outputs of that "
+                "call are NaN", fn, v);
+  return fail(MNB_ERR_INVALID_ARG, "%s: an index input was out of range (status bits 0x%x: a g_idx, perm "
+              "or block_group entry outside its range; that element was written as 0)", fn, v);
 }
 
 mnb_status mnb_dequant(mnb_weight w, int K, int N, int block_size, float* out_kn,
@@ -210,6 +215,30 @@ size_t mnb_workspace_bytes(int M, int K, int N, int block_size) {
 
 namespace {
 
+// M = 1: GEMV; M > 16: tcgen05 GEMM on the repacked operand; otherwise the small-M
+// kernel.  Shapes no specialised kernel takes go to the generic kernel.
+cudaError_t dispatch_gemm(mnb::LaunchCtx& ctx, const void* A, int M, const mnb::QWeight& q,
+                          const uint8_t* repacked, int K, int N, int bs, void* Y) {
+  cudaError_t e;
+  if (M == 1) {
+    e = run_gemv(ctx, A, q, K, N, bs, Y);
+  } else if (M > 16) {
+    e = mnb::launch_gemm_tc(ctx, A, M, q, repacked, K, N, bs, Y);
+    if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, bs, Y);
+  } else {
+    e = mnb::launch_gemm_smallm(ctx, A, M, q, K, N, bs, Y);
+    if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, bs, Y);
+  }
+  return e;
+}
+
+mnb_status check_bias(const char* fn, const void* bias, int bias_mode) {
+  if (bias_mode < 0 || bias_mode > 2)
+    return fail(MNB_ERR_INVALID_ARG, "%s: bias_mode %d must be 0, 1 or 2", fn, bias_mode);
+  if (bias_mode != 0) return check_ptr(fn, "bias", bias);
+  return MNB_OK;
+}
+
 mnb_status gemm_impl(const char* fn, const void* A, int M, mnb_weight w, const uint8_t* repacked, int K, int N,
                      int block_size, const void* bias, int bias_mode, void* workspace, size_t ws_bytes, void* Y,
                      mnb_stream stream) {
@@ -227,24 +256,12 @@ mnb_status gemm_impl(const char* fn, const void* A, int M, mnb_weight w, const u
   if (M > 16) {
     if ((st = check_ptr(fn, "repacked", repacked)) != MNB_OK) return st;
   }
-  if (bias_mode < 0 || bias_mode > 2)
-    return fail(MNB_ERR_INVALID_ARG, "%s: bias_mode %d must be 0, 1 or 2", fn, bias_mode);
-  if (bias_mode != 0 && (st = check_ptr(fn, "bias", bias)) != MNB_OK) return st;
+  if ((st = check_bias(fn, bias, bias_mode)) != MNB_OK) return st;
   mnb::LaunchCtx ctx;
   if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
   ctx.bias = bias_mode ? bias : nullptr;
   ctx.bias_mode = bias_mode;
-  cudaError_t e;
-  if (M == 1) {
-    e = run_gemv(ctx, A, q, K, N, block_size, Y);
-  } else if (M > 16) {
-    e = mnb::launch_gemm_tc(ctx, A, M, q, repacked, K, N, block_size, Y);
-    if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, block_size, Y);
-  } else {
-    e = mnb::launch_gemm_smallm(ctx, A, M, q, K, N, block_size, Y);
-    if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, block_size, Y);
-  }
-  return finish(fn, e, ctx);
+  return finish(fn, dispatch_gemm(ctx, A, M, q, repacked, K, N, block_size, Y), ctx);
 }
 
 }  // namespace
@@ -280,6 +297,162 @@ mnb_status mnb_gemv_gate_up_swiglu(const void* A, mnb_weight gate, mnb_weight up
   cudaError_t e = mnb::launch_gemv_pair_swiglu_tma(ctx, A, g, u, K, N, block_size, out);
   if (e == cudaErrorNotSupported) e = mnb::launch_gemv_pair_swiglu(ctx, A, g, u, K, N, block_size, out);
   if (e == cudaErrorNotSupported) e = mnb::launch_generic_pair_swiglu(ctx, A, g, u, K, N, block_size, out);
+  return finish(fn, e, ctx);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------
+// Act-order (g_idx) weights.
+// ------------------------------------------------------------------------------------
+
+namespace {
+
+mnb_status refuse_capture(const char* fn, mnb_stream stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cs);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(MNB_ERR_CAPTURE, "%s: refused while the stream is capturing; prepare once, before capture", fn);
+  return MNB_OK;
+}
+
+// K <= K' <= 2K holds for every plan (each non-empty group adds fewer than bs slots,
+// and there are at most K / bs groups).
+mnb_status check_prepared_k(const char* fn, int K, int Kp, int bs) {
+  mnb_status st;
+  if ((st = check_shape(fn, Kp, 1, bs)) != MNB_OK) return st;
+  if (K < 1 || K > kMaxKN || K % bs != 0)
+    return fail(MNB_ERR_INVALID_ARG, "%s: K=%d must be a multiple of block_size %d in [1, 2^24]", fn, K, bs);
+  if (Kp < K || Kp > 2 * K)
+    return fail(MNB_ERR_INVALID_ARG, "%s: K_prepared=%d must lie in [K, 2K] for K=%d", fn, Kp, K);
+  return MNB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mnb_status mnb_act_order_plan(const int32_t* g_idx, int K, int block_size, int32_t* K_prepared, int32_t* perm,
+                              int32_t* block_group) {
+  const char* fn = "mnb_act_order_plan";
+  mnb_status st;
+  if ((st = check_shape(fn, K, 1, block_size)) != MNB_OK) return st;
+  if (!g_idx) return fail(MNB_ERR_INVALID_ARG, "%s: g_idx is NULL", fn);
+  if (!K_prepared) return fail(MNB_ERR_INVALID_ARG, "%s: K_prepared is NULL", fn);
+  const int G = K / block_size;
+  std::vector<int64_t> count(G, 0);
+  for (int k = 0; k < K; ++k) {
+    const int32_t g = g_idx[k];
+    if (g < 0 || g >= G)
+      return fail(MNB_ERR_INVALID_ARG, "%s: g_idx[%d]=%d is outside 0..%d", fn, k, (int)g, G);
+    ++count[g];
+  }
+  // Each group's run starts at a block boundary; its slots past the members stay -1.
+  std::vector<int64_t> start(G + 1, 0);
+  for (int g = 0; g < G; ++g)
+    start[g + 1] = start[g] + (count[g] + block_size - 1) / block_size * block_size;
+  const int64_t kp = start[G];
+  *K_prepared = (int32_t)kp;
+  if (perm) {
+    std::vector<int64_t> cursor(start.begin(), start.end() - 1);
+    for (int64_t i = 0; i < kp; ++i) perm[i] = -1;
+    for (int k = 0; k < K; ++k) perm[cursor[g_idx[k]]++] = k;
+  }
+  if (block_group) {
+    for (int g = 0; g < G; ++g)
+      for (int64_t j = start[g] / block_size; j < start[g + 1] / block_size; ++j) block_group[j] = g;
+  }
+  g_last_error.clear();
+  return MNB_OK;
+}
+
+mnb_status mnb_dequant_gidx(mnb_weight w, const int32_t* g_idx, int K, int N, int block_size, float* out_kn,
+                            mnb_stream stream) {
+  const char* fn = "mnb_dequant_gidx";
+  mnb_status st;
+  mnb::QWeight q;
+  if ((st = check_shape(fn, K, N, block_size)) != MNB_OK) return st;
+  if ((st = check_weight(fn, w, &q)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "g_idx", g_idx)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "out_kn", out_kn)) != MNB_OK) return st;
+  mnb::LaunchCtx ctx;
+  if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
+  return finish(fn, mnb::launch_dequant_gidx(ctx, q, g_idx, K, N, block_size, out_kn), ctx);
+}
+
+mnb_status mnb_act_order_prepare(mnb_weight w, int K, int N, int block_size, const int32_t* perm,
+                                 const int32_t* block_group, int K_prepared, uint8_t* packed_out,
+                                 void* scales_out, uint8_t* zero_points_out, mnb_stream stream) {
+  const char* fn = "mnb_act_order_prepare";
+  mnb_status st;
+  mnb::QWeight q;
+  if ((st = check_shape(fn, K, N, block_size)) != MNB_OK) return st;
+  if ((st = check_prepared_k(fn, K, K_prepared, block_size)) != MNB_OK) return st;
+  if ((st = check_weight(fn, w, &q)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "perm", perm)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "block_group", block_group)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "packed_out", packed_out)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "scales_out", scales_out)) != MNB_OK) return st;
+  if (w.zero_points && (st = check_ptr(fn, "zero_points_out", zero_points_out)) != MNB_OK) return st;
+  if ((st = refuse_capture(fn, stream)) != MNB_OK) return st;
+  mnb::LaunchCtx ctx;
+  if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
+  return finish(fn,
+                mnb::launch_act_order_prepare(ctx, q, K, N, block_size, perm, block_group, K_prepared,
+                                              packed_out, scales_out, w.zero_points ? zero_points_out : nullptr),
+                ctx);
+}
+
+mnb_status mnb_act_order_gather(const void* A, int M, int K, const int32_t* perm, int K_prepared, void* A_out,
+                                mnb_stream stream) {
+  const char* fn = "mnb_act_order_gather";
+  mnb_status st;
+  if (M < 1 || M > kMaxM) return fail(MNB_ERR_INVALID_ARG, "%s: M=%d must be in [1, 2^20]", fn, M);
+  if (K < 1 || K > kMaxKN) return fail(MNB_ERR_INVALID_ARG, "%s: K=%d must be in [1, 2^24]", fn, K);
+  if (K_prepared < 8 || K_prepared % 8 != 0 || K_prepared > 2 * K)
+    return fail(MNB_ERR_INVALID_ARG, "%s: K_prepared=%d must be a positive multiple of 8, at most 2K", fn,
+                K_prepared);
+  if ((st = check_ptr(fn, "A", A)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "perm", perm)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "A_out", A_out)) != MNB_OK) return st;
+  mnb::LaunchCtx ctx;
+  if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
+  return finish(fn, mnb::launch_act_order_gather(ctx, A, M, K, perm, K_prepared, A_out), ctx);
+}
+
+size_t mnb_act_order_workspace_bytes(int M, int K_prepared) {
+  if (M < 1 || M > kMaxM || K_prepared < 1 || K_prepared > 2 * kMaxKN) return 0;
+  return (size_t)M * (size_t)K_prepared * 2;
+}
+
+mnb_status mnb_gemm_act_order(const void* A, int M, mnb_weight w, const uint8_t* repacked, const int32_t* perm,
+                              int K, int K_prepared, int N, int block_size, const void* bias, int bias_mode,
+                              void* workspace, size_t ws_bytes, void* Y, mnb_stream stream) {
+  const char* fn = "mnb_gemm_act_order";
+  mnb_status st;
+  mnb::QWeight q;
+  if ((st = check_shape(fn, K_prepared, N, block_size)) != MNB_OK) return st;
+  if ((st = check_prepared_k(fn, K, K_prepared, block_size)) != MNB_OK) return st;
+  if (M < 1 || M > kMaxM) return fail(MNB_ERR_INVALID_ARG, "%s: M=%d must be in [1, 2^20]", fn, M);
+  if ((st = check_weight(fn, w, &q)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "A", A)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "perm", perm)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "Y", Y)) != MNB_OK) return st;
+  if (M > 16 && (st = check_ptr(fn, "repacked", repacked)) != MNB_OK) return st;
+  if ((st = check_bias(fn, bias, bias_mode)) != MNB_OK) return st;
+  const size_t need = mnb_act_order_workspace_bytes(M, K_prepared);
+  if (ws_bytes < need)
+    return fail(MNB_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", fn, ws_bytes, need);
+  if ((st = check_ptr(fn, "workspace", workspace)) != MNB_OK) return st;
+  mnb::LaunchCtx ctx;
+  if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
+  cudaError_t e = mnb::launch_act_order_gather(ctx, A, M, K, perm, K_prepared, workspace);
+  if (e == cudaSuccess) {
+    ctx.bias = bias_mode ? bias : nullptr;
+    ctx.bias_mode = bias_mode;
+    e = dispatch_gemm(ctx, workspace, M, q, repacked, K_prepared, N, block_size, Y);
+  }
   return finish(fn, e, ctx);
 }
 

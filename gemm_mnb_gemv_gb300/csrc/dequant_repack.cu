@@ -25,7 +25,8 @@ struct DequantArgs {
 __global__ void __launch_bounds__(256) dequant_kernel(const DequantArgs p) {
   __shared__ float tile[64][65];
   const int tid = threadIdx.x;
-  const int n_base = blockIdx.x * 64, k_base = blockIdx.y * 64;
+  const int ntn = (p.N + 63) >> 6;
+  const int n_base = (int)(blockIdx.x % ntn) * 64, k_base = (int)(blockIdx.x / ntn) * 64;
   pdl_launch_dependents();
   pdl_wait();
   {
@@ -113,9 +114,10 @@ cudaError_t launch_dequant(LaunchCtx& ctx, const QWeight& w, int K, int N, int b
   a.G = K / bs;
   a.zrb = (a.G + 1) / 2;
   a.bs = bs;
-  dim3 grid((N + 63) / 64, (K + 63) / 64);
+  const long long tiles = (long long)((N + 63) / 64) * ((K + 63) / 64);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   ctx.variant = "dequant_f32_tile64";
-  return launch_kernel(ctx, dequant_kernel, grid, dim3(256), 0, a);
+  return launch_kernel(ctx, dequant_kernel, dim3((unsigned)tiles), dim3(256), 0, a);
 }
 
 cudaError_t launch_repack(LaunchCtx& ctx, const uint8_t* packed, int K, int N, uint8_t* out) {

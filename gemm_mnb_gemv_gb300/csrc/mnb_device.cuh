@@ -158,6 +158,7 @@ constexpr uint32_t kSpinLimit = 1u << 26;
 constexpr uint32_t kStatusFullWait = 1u;   // consumer gave up waiting for a stage
 constexpr uint32_t kStatusEmptyWait = 2u;  // producer gave up waiting for a free slot
 constexpr uint32_t kStatusMmaWait = 4u;    // tensor-core pipeline wait gave up
+constexpr uint32_t kStatusBadIndex = 8u;   // an index input (g_idx, perm, block_group) was out of range
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

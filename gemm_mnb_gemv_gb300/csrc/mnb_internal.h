@@ -28,6 +28,14 @@ struct LaunchCtx {
 // caller (api.cu).
 cudaError_t launch_dequant(LaunchCtx& ctx, const QWeight& w, int K, int N, int bs, float* out);
 cudaError_t launch_repack(LaunchCtx& ctx, const uint8_t* packed, int K, int N, uint8_t* out);
+// Act-order (g_idx): per-k-group dequant, one-time preparation, per-call activation gather.
+cudaError_t launch_dequant_gidx(LaunchCtx& ctx, const QWeight& w, const int32_t* gidx, int K, int N, int bs,
+                                float* out);
+cudaError_t launch_act_order_prepare(LaunchCtx& ctx, const QWeight& w, int K, int N, int bs, const int32_t* perm,
+                                     const int32_t* bgroup, int Kp, uint8_t* packed_out, void* scales_out,
+                                     uint8_t* zp_out);
+cudaError_t launch_act_order_gather(LaunchCtx& ctx, const void* A, int M, int K, const int32_t* perm, int Kp,
+                                    void* out);
 // Bulk-copy ring GEMV (M = 1); cudaErrorNotSupported when rows are not 16-byte multiples.
 cudaError_t launch_gemv_tma(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs,
                             void* Y);

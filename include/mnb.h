@@ -18,8 +18,9 @@
  *   dequant(B)[n, k] = (code[n, k] - zp[n, k/bs]) * scale[n, k/bs].
  *
  * Conventions shared by every entry point
- *   - Every pointer argument is device memory owned by the caller; the library keeps
- *     no reference after the call returns and allocates nothing.
+ *   - Every pointer argument is device memory owned by the caller (except where an
+ *     argument is marked HOST); the library keeps no reference after the call returns
+ *     and allocates nothing.
  *   - A and Y are fp16 (IEEE binary16, passed as raw 16-bit storage), row-major.
  *   - Every device pointer must be non-NULL (except zero_points, workspace when
  *     ws_bytes is 0, and repacked where stated) and 16-byte aligned:
@@ -165,21 +166,105 @@ MNB_API mnb_status mnb_gemv_gate_up_swiglu(const void *A, mnb_weight gate, mnb_w
                                    int block_size, void *out, mnb_stream stream);
 
 /*
+ * ---- Act-order weights (g_idx) ----
+ *
+ * MatMulNBits takes an optional int32 group index g_idx[K] (matmul_nbits.rs,
+ * MatMulNBitsKernel::run, input 4; kernel matmul_nbits_dequant_f32): the scale and zero
+ * point of column k are those of group g_idx[k] instead of group k / bs, while the code
+ * still sits in block k / bs:
+ *   dequant(B)[n, k] = (code[n, k] - zp[n, g_idx[k]]) * scale[n, g_idx[k]].
+ * The pages check every entry with a device-to-host copy on each call. Here the check
+ * happens once, on the host, when the weight is prepared (mnb_act_order_plan), and the
+ * weight is rewritten into an equivalent plain block weight of K' columns
+ * (mnb_act_order_prepare): k sorted by group, ascending k inside a group, each group's
+ * run padded with empty slots to whole blocks. Each call then gathers the activation
+ * into the same order and runs the ordinary kernels, so every per-call entry point
+ * below is capture-safe. With g_idx[k] = k / bs the prepared weight is the original.
+ */
+
+/*
+ * Dequantise with a group index per k to fp32 [K, N] (out_kn[k*N + n]), as
+ * matmul_nbits_dequant_f32 does when given group indices: element
+ * (code[n, k] - zp[n, g]) * scale[n, g], g = g_idx[k], rounded once to fp32. g_idx is
+ * device int32 [K]. An entry outside 0..K/bs-1 writes 0 for that k (the pages' kernel
+ * rule) and sets the index bit of the device status word, which mnb_check_device_status
+ * reports as MNB_ERR_INVALID_ARG.
+ */
+MNB_API mnb_status mnb_dequant_gidx(mnb_weight w, const int32_t *g_idx, int K, int N, int block_size,
+                                    float *out_kn, mnb_stream stream);
+
+/*
+ * Host-only planning step (no GPU work). g_idx is HOST int32 [K]; every entry must lie
+ * in 0..K/bs-1, else MNB_ERR_INVALID_ARG names the first bad entry (the operator's own
+ * check, matmul_nbits.rs). Writes *K_prepared = K' = bs * sum_g ceil(count_g / bs), with
+ * K <= K' <= 2K (K' = K when every group has exactly bs members, the act-order
+ * quantisation case). If perm is not NULL it receives K' entries (host int32): perm[k']
+ * = the source column of prepared column k', or -1 for an empty slot. If block_group is
+ * not NULL it receives K'/bs entries: the group of each prepared block. Call once with
+ * NULL arrays to learn K', or size both for the 2K worst case.
+ */
+MNB_API mnb_status mnb_act_order_plan(const int32_t *g_idx, int K, int block_size, int32_t *K_prepared,
+                                      int32_t *perm, int32_t *block_group);
+
+/*
+ * Write the prepared weight (device buffers owned by the caller, same block_size, K'
+ * columns): packed_out [N, K'/2] bytes with codes code[n, perm[k']] (the block's zero
+ * point at an empty slot, so its weight is 0); scales_out [N, K'/bs] of w.scales_dtype,
+ * scales_out[n, j] = scales[n, block_group[j]]; zero_points_out [N, ceil(K'/bs/2)] bytes
+ * (nibbles as in MatMulNBits, the unused high nibble of an odd count 0), required when w
+ * has zero points and ignored otherwise (the prepared weight then has none either).
+ * perm [K'] and block_group [K'/bs] are device copies of mnb_act_order_plan's output.
+ * For M > 16 repack packed_out with mnb_repack(packed_out, K', N, block_size, ...).
+ * Runs once per weight, so it is refused with MNB_ERR_CAPTURE while `stream` captures.
+ */
+MNB_API mnb_status mnb_act_order_prepare(mnb_weight w, int K, int N, int block_size, const int32_t *perm,
+                                         const int32_t *block_group, int K_prepared, uint8_t *packed_out,
+                                         void *scales_out, uint8_t *zero_points_out, mnb_stream stream);
+
+/*
+ * A_out[m, k'] = A[m, perm[k']] for m < M, k' < K', and +0 where perm[k'] = -1 (fp16,
+ * row-major; A is [M, K], A_out is [M, K']). perm is device int32 [K'] and K' a
+ * multiple of 8 no larger than 2K. Any other perm entry writes 0 and sets the index
+ * bit of the device status word.
+ */
+MNB_API mnb_status mnb_act_order_gather(const void *A, int M, int K, const int32_t *perm, int K_prepared,
+                                        void *A_out, mnb_stream stream);
+
+/* Workspace bytes mnb_gemm_act_order needs: M * K' * 2 (the gathered activation). */
+MNB_API size_t mnb_act_order_workspace_bytes(int M, int K_prepared);
+
+/*
+ * Y[M, N] = A[M, K] . dequant_g_idx(B)^T for an act-order weight, with the bias modes of
+ * mnb_gemm_bias. `w` and `repacked` are the PREPARED weight (K' columns; `repacked`
+ * needed for M > 16 as in mnb_gemm); perm is the device copy of the plan's perm. The call
+ * gathers A into `workspace` (at least mnb_act_order_workspace_bytes(M, K') bytes,
+ * contents need no initialisation, overwritten by each call) and then runs mnb_gemm's
+ * kernel for (M, K', N) on it. Calls that share one workspace must be ordered on one
+ * stream. Tolerance as mnb_gemm, with the bound taken over the g_idx weights.
+ */
+MNB_API mnb_status mnb_gemm_act_order(const void *A, int M, mnb_weight w, const uint8_t *repacked,
+                                      const int32_t *perm, int K, int K_prepared, int N, int block_size,
+                                      const void *bias, int bias_mode, void *workspace, size_t ws_bytes,
+                                      void *Y, mnb_stream stream);
+
+/*
  * Programmatic dependent launch. With `enable` != 0, later calls on this host thread
  * launch their kernels with programmatic stream serialisation: a kernel may start while
  * the previous kernel on the stream is still running, and it streams its weight, scale
- * and zero-point buffers before waiting for that kernel to finish; it reads A and writes
- * Y only after the wait. Enable it only when no earlier work on the stream writes the
- * weight buffers (weights that stay constant during inference). Default: off.
+ * and zero-point buffers (and an act-order perm) before waiting for that kernel to
+ * finish; it reads A and writes Y only after the wait. Enable it only when no earlier
+ * work on the stream writes those buffers (weights that stay constant during
+ * inference). Default: off.
  */
 MNB_API void mnb_set_programmatic_launch(int enable);
 
 /*
  * Reads and clears the device status word. Kernels that wait on shared-memory barriers
  * bound every wait; one that gives up sets a bit in this word, writes NaN outputs and
- * returns instead of hanging. Returns MNB_ERR_TIMEOUT (with the bits in the message) if
- * any bit was set since the last check, else MNB_OK. Synchronises the current device, so
- * it must not be called while a stream is being captured.
+ * returns instead of hanging. The act-order kernels set another bit for an index input
+ * out of range. Returns MNB_ERR_TIMEOUT (with the bits in the message) if a wait gave
+ * up, MNB_ERR_INVALID_ARG if only the index bit is set, else MNB_OK. Synchronises the
+ * current device, so it must not be called while a stream is being captured.
  */
 MNB_API mnb_status mnb_check_device_status(void);
 

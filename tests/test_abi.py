@@ -117,3 +117,74 @@ def test_swiglu_and_dequant_and_repack_validation(lib):
     assert lib.mnb_dequant(w, 256, 128, 32, ctypes.c_void_p(66), None) == mnb.MNB_ERR_MISALIGNED
     assert lib.mnb_repack(None, 256, 128, 32, ctypes.c_void_p(64), None) == mnb.MNB_ERR_INVALID_ARG
     assert lib.mnb_repack(ctypes.c_void_p(64), 250, 128, 32, ctypes.c_void_p(64), None) == mnb.MNB_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------------------
+# Act-order: the planning step is host code, so it runs here against the oracle.
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("kind,K,bs", [("act_order", 4096, 128), ("uneven", 1024, 32), ("identity", 512, 64),
+                                       ("uneven", 256, 16), ("act_order", 14336, 32)])
+def test_act_order_plan_matches_oracle(lib, kind, K, bs):
+    import numpy as np
+    import gemm_mnb_gemv_gb300 as mnb
+    import mnb_synth as syn
+    from oracle import mnb_oracle as orc
+    wl = syn.custom(f"abi_plan_{kind}_{K}_{bs}", 1, K, 8, bs)
+    g_idx = syn.make_g_idx(wl, kind)
+    kp, perm, bg = mnb.mnb_act_order_plan(g_idx, K, bs)
+    kp_ref, perm_ref, bg_ref = orc.act_order_plan(g_idx, K, bs)
+    assert kp == kp_ref and K <= kp <= 2 * K
+    np.testing.assert_array_equal(perm, perm_ref)
+    np.testing.assert_array_equal(bg, bg_ref)
+
+
+def test_act_order_plan_worst_case_and_errors(lib):
+    import numpy as np
+    import gemm_mnb_gemv_gb300 as mnb
+    K, bs = 256, 16
+    g_idx = np.arange(K, dtype=np.int32) % (K // bs)   # 16 groups of 16, interleaved: K' = K
+    assert mnb.mnb_act_order_plan(g_idx, K, bs)[0] == K
+    g_idx = np.zeros(K, dtype=np.int32)
+    g_idx[: K // bs] = np.arange(K // bs)               # every group gets 1 member, group 0 gets 241
+    kp, perm, bg = mnb.mnb_act_order_plan(g_idx, K, bs)
+    assert kp == 16 * 16 + 15 * 16 and kp <= 2 * K
+    bad = np.zeros(K, dtype=np.int32)
+    bad[77] = K // bs
+    with pytest.raises(mnb.MnbError, match=r"g_idx\[77\]=16 is outside 0..16"):
+        mnb.mnb_act_order_plan(bad, K, bs)
+    bad[77] = -2
+    with pytest.raises(mnb.MnbError, match=r"g_idx\[77\]=-2"):
+        mnb.mnb_act_order_plan(bad, K, bs)
+    kp = ctypes.c_int32(0)
+    assert lib.mnb_act_order_plan(None, K, bs, ctypes.byref(kp), None, None) == mnb.MNB_ERR_INVALID_ARG
+    gp = g_idx.ctypes.data_as(ctypes.c_void_p)
+    assert lib.mnb_act_order_plan(gp, K, bs, None, None, None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_act_order_plan(gp, 250, bs, ctypes.byref(kp), None, None) == mnb.MNB_ERR_UNSUPPORTED
+
+
+def test_act_order_entry_validation_without_gpu(lib):
+    import gemm_mnb_gemv_gb300 as mnb
+    w = _w(16, 32, 0, None)
+    p = ctypes.c_void_p
+    # K' outside [K, 2K]
+    assert lib.mnb_gemm_act_order(p(64), 1, w, None, p(64), 256, 544, 128, 32, None, 0, p(64), 1 << 20,
+                                  p(64), None) == mnb.MNB_ERR_INVALID_ARG
+    assert "K_prepared" in mnb.mnb_last_error()
+    # workspace too small
+    assert lib.mnb_gemm_act_order(p(64), 4, w, None, p(64), 256, 256, 128, 32, None, 0, p(64), 100,
+                                  p(64), None) == mnb.MNB_ERR_INVALID_ARG
+    assert "workspace" in mnb.mnb_last_error()
+    assert mnb.mnb_act_order_workspace_bytes(4, 256) == 4 * 256 * 2
+    # perm NULL / misaligned
+    assert lib.mnb_gemm_act_order(p(64), 1, w, None, None, 256, 256, 128, 32, None, 0, p(64), 512,
+                                  p(64), None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_act_order_gather(p(64), 1, 256, p(68), 256, p(64), None) == mnb.MNB_ERR_MISALIGNED
+    assert lib.mnb_act_order_gather(p(64), 1, 256, p(64), 260, p(64), None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_dequant_gidx(w, None, 256, 128, 32, p(64), None) == mnb.MNB_ERR_INVALID_ARG
+    # prepare needs zero_points_out when the weight has zero points
+    wz = _w(16, 32, 0, 48)
+    assert lib.mnb_act_order_prepare(wz, 256, 128, 32, p(64), p(64), 256, p(64), p(64), None,
+                                     None) == mnb.MNB_ERR_INVALID_ARG
+    assert "zero_points_out" in mnb.mnb_last_error()
