@@ -10,7 +10,8 @@ The names match the C entry points: ``mnb_dequant``, ``mnb_repacked_bytes``,
 ``mnb_repack``, ``mnb_gemv``, ``mnb_workspace_bytes``, ``mnb_gemm``,
 ``mnb_gemm_bias``, ``mnb_gemv_gate_up_swiglu``, ``mnb_dequant_gidx``,
 ``mnb_act_order_plan``, ``mnb_act_order_prepare``, ``mnb_act_order_gather``,
-``mnb_act_order_workspace_bytes``, ``mnb_gemm_act_order``, ``mnb_set_programmatic_launch``,
+``mnb_act_order_workspace_bytes``, ``mnb_gemm_act_order``, ``mnb_gemm_act_order_noalloc``,
+``mnb_set_programmatic_launch``,
 ``mnb_check_device_status``,
 ``mnb_last_error``,
 ``mnb_last_variant``, ``mnb_version``.
@@ -71,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mnb_act_order_workspace_bytes": (c_size, [c_int, c_int]),
         "mnb_gemm_act_order": (c_int, [vp, c_int, MnbWeight, vp, vp, c_int, c_int, c_int, c_int, vp, c_int, vp,
                                        c_size, vp, vp]),
+        "mnb_gemm_act_order_noalloc": (c_int, [vp, c_int, MnbWeight, vp, vp, c_int, c_int, c_int, c_int, vp,
+                                               c_int, vp, vp]),
         "mnb_set_programmatic_launch": (None, [c_int]),
         "mnb_check_device_status": (c_int, []),
         "mnb_last_error": (ctypes.c_char_p, []),
@@ -364,4 +367,25 @@ def mnb_gemm_act_order(A, packed, scales, zero_points, perm, K: int, K_prepared:
     _raise(lib.mnb_gemm_act_order(_ptr(A), M, w, _ptr(repacked), _ptr(perm), K, K_prepared, N, block_size,
                                   _ptr(bias), bias_mode, _ptr(workspace), ws_bytes, _ptr(out),
                                   _stream_handle(stream)))
+    return out
+
+
+def mnb_gemm_act_order_noalloc(A, packed, scales, zero_points, perm, K: int, K_prepared: int, N: int,
+                               block_size: int, repacked=None, bias=None, bias_mode: int = MNB_BIAS_NONE, out=None,
+                               stream=None):
+    """``mnb_gemm_act_order`` with the library's static scratch (M * K' * 2 <= 8 MiB) instead of a
+    workspace; pass ``out`` to keep the call free of allocations."""
+    torch = _torch()
+    lib = load_library()
+    _check_dev("A", A, torch.float16)
+    _check_dev("perm", perm, torch.int32)
+    _check_dev("bias", bias, torch.float16)
+    _check_dev("repacked", repacked, torch.uint8)
+    M = A.numel() // K
+    w = _weight(packed, scales, zero_points)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check_dev("out", out, torch.float16)
+    _raise(lib.mnb_gemm_act_order_noalloc(_ptr(A), M, w, _ptr(repacked), _ptr(perm), K, K_prepared, N,
+                                          block_size, _ptr(bias), bias_mode, _ptr(out), _stream_handle(stream)))
     return out

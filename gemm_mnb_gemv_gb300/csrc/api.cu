@@ -457,3 +457,82 @@ mnb_status mnb_gemm_act_order(const void* A, int M, mnb_weight w, const uint8_t*
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------
+// Act-order product for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc: a plugin inside a host framework that owns all
+// device memory through its own allocator and hands the plugin no workspace, or a
+// latency-critical loop where cudaMalloc's implicit device synchronisation is not
+// allowed. mnb_gemm_act_order_noalloc takes its scratch (the gathered activation
+// A'[M, K'] in fp16) from the fixed array below instead of a caller workspace.
+// ------------------------------------------------------------------------------------
+
+// 8 MiB: M * K' * 2 bytes must fit (e.g. M = 16 with K' up to 262144, M = 1024 with
+// K' = 4096). Every GPU that loads the library holds this array until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[128] = {};
+
+// Once per device, with that device current: the device address of g_noalloc_scratch
+// (in host code the array's name is only a stand-in for the symbol, not an address).
+mnb_status noalloc_scratch(const char* fn, void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  if (dev < 0 || dev >= 128) return fail(MNB_ERR_UNSUPPORTED, "%s: device ordinal %d is above 127", fn, dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(fn, e);
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MNB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mnb_status mnb_gemm_act_order_noalloc(const void* A, int M, mnb_weight w, const uint8_t* repacked,
+                                      const int32_t* perm, int K, int K_prepared, int N, int block_size,
+                                      const void* bias, int bias_mode, void* Y, mnb_stream stream) {
+  const char* fn = "mnb_gemm_act_order_noalloc";
+  mnb_status st;
+  mnb::QWeight q;
+  if ((st = check_shape(fn, K_prepared, N, block_size)) != MNB_OK) return st;
+  if ((st = check_prepared_k(fn, K, K_prepared, block_size)) != MNB_OK) return st;
+  if (M < 1 || M > kMaxM) return fail(MNB_ERR_INVALID_ARG, "%s: M=%d must be in [1, 2^20]", fn, M);
+  if ((st = check_weight(fn, w, &q)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "A", A)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "perm", perm)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "Y", Y)) != MNB_OK) return st;
+  if (M > 16 && (st = check_ptr(fn, "repacked", repacked)) != MNB_OK) return st;
+  if ((st = check_bias(fn, bias, bias_mode)) != MNB_OK) return st;
+  const size_t need = (size_t)M * (size_t)K_prepared * 2;
+  if (need > kNoAllocScratchBytes)
+    return fail(MNB_ERR_UNSUPPORTED, "%s: M=%d x K_prepared=%d needs %zu scratch bytes; the library's static "
+                "scratch holds %zu (use mnb_gemm_act_order with a workspace)", fn, M, K_prepared, need,
+                kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(fn, &scratch)) != MNB_OK) return st;
+  mnb::LaunchCtx ctx;
+  if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
+  // The gather writes every byte of A'[M, K'] that the product then reads, padding
+  // slots included, so nothing left in the array by an earlier call is used.
+  cudaError_t e = mnb::launch_act_order_gather(ctx, A, M, K, perm, K_prepared, scratch);
+  if (e == cudaSuccess) {
+    ctx.bias = bias_mode ? bias : nullptr;
+    ctx.bias_mode = bias_mode;
+    e = dispatch_gemm(ctx, scratch, M, q, repacked, K_prepared, N, block_size, Y);
+  }
+  return finish(fn, e, ctx);
+}
+
+}  // extern "C"

@@ -248,6 +248,27 @@ MNB_API mnb_status mnb_gemm_act_order(const void *A, int M, mnb_weight w, const 
                                       void *Y, mnb_stream stream);
 
 /*
+ * mnb_gemm_act_order without a workspace, for callers that cannot allocate device
+ * memory (a plugin inside a host framework that owns all device memory and hands it no
+ * workspace, or a loop where cudaMalloc's implicit synchronisation is not allowed). The
+ * paper has no counterpart: this entry point is this library's own.
+ * Same arguments and result as mnb_gemm_act_order minus workspace/ws_bytes. The
+ * gathered activation (M * K' * 2 bytes) lives in a static device array of 8 MiB
+ * (8388608 bytes) inside the library, held on every GPU that loads the library until
+ * the process exits; a larger M * K' gives MNB_ERR_UNSUPPORTED. The call allocates
+ * nothing. Its first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call before any
+ * stream capture. All calls share the one array and it keeps the last call's contents
+ * (each call overwrites everything it reads, so nothing needs clearing): calls that
+ * may overlap on the GPU (different streams, or threads without ordering) race on it,
+ * so order them on one stream.
+ */
+MNB_API mnb_status mnb_gemm_act_order_noalloc(const void *A, int M, mnb_weight w, const uint8_t *repacked,
+                                              const int32_t *perm, int K, int K_prepared, int N,
+                                              int block_size, const void *bias, int bias_mode, void *Y,
+                                              mnb_stream stream);
+
+/*
  * Programmatic dependent launch. With `enable` != 0, later calls on this host thread
  * launch their kernels with programmatic stream serialisation: a kernel may start while
  * the previous kernel on the stream is still running, and it streams its weight, scale
