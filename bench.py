@@ -321,6 +321,33 @@ class DeviceBench:
                 "gbps": call_bytes(wl) / (us * 1e3), "tflops": call_flops(wl) / (us * 1e6),
                 "copies": ncopy, "variant": mnb.mnb_last_variant()}
 
+    def gemm_f32(self, wl, steps, warmup, sampler, calls):
+        """fp32 activations and output: the fp32 GEMV at M = 1, the split-activation
+        kernels (split pass + GEMM, two launches) for M >= 2."""
+        torch, mnb = self.torch, self.mnb
+        per_copy = weight_bytes(wl) + wl.M * wl.K * 4
+        ncopy = self.copies_for(per_copy)
+        _, copies = self.upload_weights(wl, "B", ncopy)
+        A0 = torch.from_numpy(syn.make_activation_f32(wl)).to(self.dev)
+        As = [A0] + [A0.clone() for _ in range(ncopy - 1)]
+        rps = [mnb.mnb_repack(c[0], wl.K, wl.N, wl.block_size) if wl.M > 8 else None for c in copies]
+        Y = torch.empty((wl.M, wl.N), dtype=torch.float32, device=self.dev)
+        need = mnb.mnb_workspace_bytes_f32(wl.M, wl.K, wl.N, wl.block_size)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.dev)
+
+        def rec():
+            for i in range(calls):
+                j = i % ncopy
+                mnb.mnb_gemm_f32(As[j], *copies[j], wl.K, wl.N, wl.block_size, repacked=rps[j],
+                                 workspace=ws, out=Y)
+
+        launches = calls if wl.M == 1 else 2 * calls
+        ms, _ = self.time_graph(rec, launches, steps, warmup, sampler)
+        us = ms * 1e3 / calls
+        nbytes = weight_bytes(wl) + 4 * wl.M * wl.K + 4 * wl.M * wl.N
+        return {"workload": wl.name + "_f32act", "M": wl.M, "us_per_call": us, "gbps": nbytes / (us * 1e3),
+                "tflops": call_flops(wl) / (us * 1e6), "copies": ncopy, "variant": mnb.mnb_last_variant()}
+
     def e2e_gemv(self, res, steps):
         """Host activations in, host result out, around the same graph of 1000 calls."""
         torch = self.torch
@@ -457,6 +484,10 @@ def run_single(db, name, steps, warmup):
         return db.mlp_chain(steps, warmup, None)
     if name == "act_order_attn":
         return db.act_order(W[HEADLINE], steps, warmup, None)
+    if name == "f32_attn":
+        return db.gemm_f32(W[HEADLINE], steps, warmup, None, calls=200)
+    if name == "f32_prefill":
+        return db.gemm_f32(W["prefill_m2048_k4096_n14336"], steps, warmup, None, calls=5)
     if name == "prefill":
         return db.gemm(W["prefill_m2048_k4096_n14336"], steps, warmup, None, calls=9, repacked=True)
     raise SystemExit(f"unknown workload {name}")
@@ -473,7 +504,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     help="time one workload only (attn, gate_up, down, verify_m2/4/8/16, prefill, mlp_chain, "
-                         "act_order_attn) "
+                         "act_order_attn, f32_attn, f32_prefill) "
                          "and print its record; for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -529,6 +560,8 @@ def main():
                                     calls=9, repacked=True)
         extras["mlp_chain"] = db.mlp_chain(10, 3, sampler)
         extras["act_order_attn"] = db.act_order(wl, 20, 3, sampler)
+        extras["f32_attn"] = db.gemm_f32(wl, 20, 3, sampler, calls=200)
+        extras["f32_prefill"] = db.gemm_f32(syn.WORKLOADS["prefill_m2048_k4096_n14336"], 5, 3, sampler, calls=5)
     for k, v in extras.items():
         log(f"{k}: {v['us_per_call']:.3f} us/call, {v.get('gbps', 0):.1f} GB/s, "
             f"{v.get('tflops', 0):.1f} TFLOP/s ({v['variant']})")

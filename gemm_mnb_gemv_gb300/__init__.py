@@ -8,7 +8,8 @@ output tensor is not passed, the binding allocates it with torch before the call
 
 The names match the C entry points: ``mnb_dequant``, ``mnb_repacked_bytes``,
 ``mnb_repack``, ``mnb_gemv``, ``mnb_workspace_bytes``, ``mnb_gemm``,
-``mnb_gemm_bias``, ``mnb_gemv_gate_up_swiglu``, ``mnb_dequant_gidx``,
+``mnb_gemm_bias``, ``mnb_gemv_gate_up_swiglu``, ``mnb_workspace_bytes_f32``, ``mnb_gemm_f32``,
+``mnb_dequant_gidx``,
 ``mnb_act_order_plan``, ``mnb_act_order_prepare``, ``mnb_act_order_gather``,
 ``mnb_act_order_workspace_bytes``, ``mnb_gemm_act_order``, ``mnb_gemm_act_order_noalloc``,
 ``mnb_set_programmatic_launch``,
@@ -65,6 +66,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mnb_gemm": (c_int, [vp, c_int, MnbWeight, vp, c_int, c_int, c_int, vp, c_size, vp, vp]),
         "mnb_gemv_gate_up_swiglu": (c_int, [vp, MnbWeight, MnbWeight, c_int, c_int, c_int, vp, vp]),
         "mnb_gemm_bias": (c_int, [vp, c_int, MnbWeight, vp, c_int, c_int, c_int, vp, c_int, vp, c_size, vp, vp]),
+        "mnb_workspace_bytes_f32": (c_size, [c_int, c_int, c_int, c_int]),
+        "mnb_gemm_f32": (c_int, [vp, c_int, MnbWeight, vp, c_int, c_int, c_int, vp, vp, c_size, vp, vp]),
         "mnb_dequant_gidx": (c_int, [MnbWeight, vp, c_int, c_int, c_int, vp, vp]),
         "mnb_act_order_plan": (c_int, [vp, c_int, c_int, vp, vp, vp]),
         "mnb_act_order_prepare": (c_int, [MnbWeight, c_int, c_int, c_int, vp, vp, c_int, vp, vp, vp, vp]),
@@ -262,6 +265,37 @@ def mnb_gemv_gate_up_swiglu(A, gate, up, K: int, N: int, block_size: int, out=No
     _check_dev("out", out, torch.float16)
     _raise(lib.mnb_gemv_gate_up_swiglu(_ptr(A), wg, wu, K, N, block_size, _ptr(out),
                                        _stream_handle(stream)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# fp32 activations
+# ---------------------------------------------------------------------------
+
+
+def mnb_workspace_bytes_f32(M: int, K: int, N: int, block_size: int) -> int:
+    return int(load_library().mnb_workspace_bytes_f32(M, K, N, block_size))
+
+
+def mnb_gemm_f32(A, packed, scales, zero_points, K: int, N: int, block_size: int, repacked=None, bias=None,
+                 workspace=None, out=None, stream=None):
+    """fp32 ``[M, N]`` = A (fp32 ``[M, K]``) times the dequantised weight (+ fp32 bias ``[N]``)."""
+    torch = _torch()
+    lib = load_library()
+    _check_dev("A", A, torch.float32)
+    _check_dev("bias", bias, torch.float32)
+    _check_dev("repacked", repacked, torch.uint8)
+    M = A.numel() // K
+    w = _weight(packed, scales, zero_points)
+    need = mnb_workspace_bytes_f32(M, K, N, block_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _check_dev("out", out, torch.float32)
+    _raise(lib.mnb_gemm_f32(_ptr(A), M, w, _ptr(repacked), K, N, block_size, _ptr(bias), _ptr(workspace),
+                            ws_bytes, _ptr(out), _stream_handle(stream)))
     return out
 
 

@@ -303,6 +303,58 @@ mnb_status mnb_gemv_gate_up_swiglu(const void* A, mnb_weight gate, mnb_weight up
 }  // extern "C"
 
 // ------------------------------------------------------------------------------------
+// fp32 activations.
+// ------------------------------------------------------------------------------------
+
+extern "C" {
+
+size_t mnb_workspace_bytes_f32(int M, int K, int N, int block_size) {
+  (void)N;
+  (void)block_size;
+  if (M < 2 || M > kMaxM || K < 1 || K > kMaxKN) return 0;
+  const size_t split = (size_t)4 * (size_t)M * (size_t)K;  // 2M fp16 rows of K
+  return split + ((size_t)4 * (size_t)M + 15) / 16 * 16;   // + M exponents
+}
+
+mnb_status mnb_gemm_f32(const float* A, int M, mnb_weight w, const uint8_t* repacked, int K, int N, int block_size,
+                        const float* bias, void* workspace, size_t ws_bytes, float* Y, mnb_stream stream) {
+  const char* fn = "mnb_gemm_f32";
+  mnb_status st;
+  mnb::QWeight q;
+  if ((st = check_shape(fn, K, N, block_size)) != MNB_OK) return st;
+  if (M < 1 || M > kMaxM) return fail(MNB_ERR_INVALID_ARG, "%s: M=%d must be in [1, 2^20]", fn, M);
+  if ((st = check_weight(fn, w, &q)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "A", A)) != MNB_OK) return st;
+  if ((st = check_ptr(fn, "Y", Y)) != MNB_OK) return st;
+  if (bias && !aligned16(bias)) return fail(MNB_ERR_MISALIGNED, "%s: bias is not 16-byte aligned", fn);
+  const size_t need = mnb_workspace_bytes_f32(M, K, N, block_size);
+  if (ws_bytes < need)
+    return fail(MNB_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", fn, ws_bytes, need);
+  if (need > 0 && (st = check_ptr(fn, "workspace", workspace)) != MNB_OK) return st;
+  if (2 * M > 16 && (st = check_ptr(fn, "repacked", repacked)) != MNB_OK) return st;
+  mnb::LaunchCtx ctx;
+  if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
+  cudaError_t e;
+  if (M == 1) {
+    e = mnb::launch_gemv_f32_tma(ctx, A, q, K, N, block_size, Y, bias);
+  } else {
+    uint8_t* a2 = static_cast<uint8_t*>(workspace);
+    int* rexp = reinterpret_cast<int*>(a2 + (size_t)4 * M * K);
+    e = mnb::launch_split_f32(ctx, A, M, K, a2, rexp);
+    if (e == cudaSuccess) {
+      if (2 * M <= 16)
+        e = mnb::launch_gemm_smallm_f32split(ctx, a2, M, q, K, N, block_size, Y, bias, rexp);
+      else
+        e = mnb::launch_gemm_tc_f32split(ctx, a2, M, q, repacked, K, N, block_size, Y, bias, rexp);
+    }
+  }
+  if (e == cudaErrorNotSupported) e = mnb::launch_generic_f32(ctx, A, M, q, K, N, block_size, Y, bias);
+  return finish(fn, e, ctx);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------
 // Act-order (g_idx) weights.
 // ------------------------------------------------------------------------------------
 

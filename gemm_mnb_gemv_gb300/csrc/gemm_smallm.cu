@@ -50,6 +50,12 @@ struct SmArgs {
   uint32_t* status;
   const __half* bias;
   int bias_mode;
+  // fp32 output (F32): A holds 2 * Mout rows, row 2m = hi and row 2m + 1 = lo of fp32 row m
+  // scaled by 2^-rexp[m]; Yf[m, n] = 2^rexp[m] * (y[2m, n] + y[2m + 1, n]) + biasf[n].
+  int Mout;
+  float* Yf;
+  const float* biasf;
+  const int* rexp;
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -67,7 +73,19 @@ __device__ __forceinline__ void group_bar(int gi) {
   asm volatile("bar.sync %0, %1;" ::"r"(2 + gi), "n"(kGW * 32) : "memory");
 }
 
-template <int MSETS, bool S16, bool ZP>
+// Fixed-order sum over the K slices of the staged partials of activation row m, weight row
+// `row` of the tile.
+template <int MSETS>
+__device__ __forceinline__ float slice_sum(const float (&red)[kGW][MSETS][32][4], int row, int m) {
+  const int s = m >> 3, mm = m & 7;
+  const int l = (row & 7) * 4 + (mm >> 1), j = ((row >> 3) << 1) + (mm & 1);
+  float v = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kGW; ++w) v += red[w][s][l][j];
+  return v;
+}
+
+template <int MSETS, bool S16, bool ZP, bool F32 = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
@@ -227,6 +245,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
       group_bar(gi);
       // Fixed-order sum over the K slices; one thread per (row, m).
       const int n0 = (t_begin + i) * kRows;
+      if constexpr (F32) {
+        for (int e = gw * 32 + lane; e < kRows * p.Mout; e += kGW * 32) {
+          const int row = e % kRows, m = e / kRows;
+          const float v = slice_sum<MSETS>(red[gi], row, 2 * m) + slice_sum<MSETS>(red[gi], row, 2 * m + 1);
+          const int n = n0 + row;
+          if (n < p.N) {
+            p.Yf[(long long)m * p.N + n] =
+                failed ? __uint_as_float(0x7fc00000u) : ldexpf(v, p.rexp[m]) + (p.biasf ? p.biasf[n] : 0.0f);
+          }
+        }
+        group_bar(gi);
+        continue;
+      }
       for (int e = gw * 32 + lane; e < kRows * 8 * MSETS; e += kGW * 32) {
         const int row = e % kRows, m = e / kRows;
         const int s = m >> 3, mm = m & 7;
@@ -246,16 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
 
 using SmKernel = void (*)(const SmArgs);
 
-template <int MSETS>
+template <int MSETS, bool F32>
 SmKernel pick(bool s16, bool zp) {
-  if (s16) return zp ? gemm_smallm_kernel<MSETS, true, true> : gemm_smallm_kernel<MSETS, true, false>;
-  return zp ? gemm_smallm_kernel<MSETS, false, true> : gemm_smallm_kernel<MSETS, false, false>;
+  if (s16) return zp ? gemm_smallm_kernel<MSETS, true, true, F32> : gemm_smallm_kernel<MSETS, true, false, F32>;
+  return zp ? gemm_smallm_kernel<MSETS, false, true, F32> : gemm_smallm_kernel<MSETS, false, false, F32>;
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
-                               void* Y) {
+cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
+                               void* Y, int Mout, float* Yf, const float* biasf, const int* rexp) {
   if (M < 2 || M > 16 || bs < 32 || K % 32 != 0) return cudaErrorNotSupported;
   SmArgs a = {};
   a.A = static_cast<const __half*>(A);
@@ -286,12 +315,32 @@ cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeig
   a.status = ctx.status;
   a.bias = static_cast<const __half*>(ctx.bias);
   a.bias_mode = ctx.bias_mode;
+  a.Mout = Mout;
+  a.Yf = Yf;
+  a.biasf = biasf;
+  a.rexp = rexp;
+  const bool f32 = Yf != nullptr;
   const size_t smem = (size_t)a.stages * a.stage_bytes + xbytes;
-  SmKernel kern = msets == 1 ? pick<1>(w.scales_f16 != 0, w.zp != nullptr) : pick<2>(w.scales_f16 != 0, w.zp != nullptr);
+  const bool s16 = w.scales_f16 != 0, zp = w.zp != nullptr;
+  SmKernel kern = msets == 1 ? (f32 ? pick<1, true>(s16, zp) : pick<1, false>(s16, zp))
+                             : (f32 ? pick<2, true>(s16, zp) : pick<2, false>(s16, zp));
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ctx.variant = "gemm_smallm_mma16816";
+  ctx.variant = f32 ? "gemm_smallm_mma16816_f32split" : "gemm_smallm_mma16816";
   return launch_kernel(ctx, kern, dim3(grid), dim3(kThreads), smem, a);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
+                               void* Y) {
+  return launch_smallm_impl(ctx, A, M, w, K, N, bs, Y, M, nullptr, nullptr, nullptr);
+}
+
+cudaError_t launch_gemm_smallm_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w, int K, int N,
+                                        int bs, float* Y, const float* bias, const int* rexp) {
+  if (M < 1 || 2 * M > 16) return cudaErrorNotSupported;
+  return launch_smallm_impl(ctx, A2, 2 * M, w, K, N, bs, nullptr, M, Y, bias, rexp);
 }
 
 }  // namespace mnb

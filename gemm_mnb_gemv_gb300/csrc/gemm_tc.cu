@@ -59,6 +59,14 @@ struct TcArgs {
   uint32_t* status;
   const __half* bias;
   int bias_mode;
+  // fp32 output (F32): the activation operand has 2 * Mout rows, row 2m = hi and row
+  // 2m + 1 = lo of fp32 row m scaled by 2^-rexp[m]; the two accumulator columns of a
+  // pair sit next to each other in one epilogue thread, which stores
+  // Yf[m, n] = 2^rexp[m] * (acc[2m] + acc[2m + 1]) + biasf[n].
+  int Mout;
+  float* Yf;
+  const float* biasf;
+  const int* rexp;
 };
 
 __device__ __forceinline__ uint32_t zp_byte(const TcArgs& p, int n, int byte_idx) {
@@ -66,6 +74,7 @@ __device__ __forceinline__ uint32_t zp_byte(const TcArgs& p, int n, int byte_idx
   return ld_nc_u8(p.zp + (long long)n * p.zrb + byte_idx);
 }
 
+template <bool F32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const TcArgs p, const __grid_constant__ CUtensorMap tmap_a) {
   extern __shared__ uint8_t smem_raw[];
@@ -364,11 +373,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (nval) {
         const int m0 = mt * kTileM + half * 128;
-        __half* yc = p.Y + n;
+        if constexpr (F32) {
+          const float b = p.biasf ? p.biasf[n] : 0.0f;
+          float* yc = p.Yf + n;
+          const int mo0 = m0 >> 1;  // m0 is even: columns 2i and 2i + 1 are one fp32 row
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          const int m = m0 + i;
-          if (m < p.M) yc[(long long)m * p.N] = round_out(acc[i], p.bias, n, p.bias_mode);
+          for (int i = 0; i < 64; ++i) {
+            const int mo = mo0 + i;
+            if (mo < p.Mout) yc[(long long)mo * p.N] = ldexpf(acc[2 * i] + acc[2 * i + 1], p.rexp[mo]) + b;
+          }
+        } else {
+          __half* yc = p.Y + n;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            const int m = m0 + i;
+            if (m < p.M) yc[(long long)m * p.N] = round_out(acc[i], p.bias, n, p.bias_mode);
+          }
         }
       }
     }
@@ -380,7 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n >= p.N) continue;
         for (int i = 0; i < 128; ++i) {
           const int m = mt * kTileM + half * 128 + i;
-          if (m < p.M) p.Y[(long long)m * p.N + n] = __ushort_as_half(0x7e00);
+          if constexpr (F32) {
+            if ((m & 1) == 0 && (m >> 1) < p.Mout) p.Yf[(long long)(m >> 1) * p.N + n] = __uint_as_float(0x7fc00000u);
+          } else {
+            if (m < p.M) p.Y[(long long)m * p.N + n] = __ushort_as_half(0x7e00);
+          }
         }
       }
     }
@@ -412,8 +436,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 size_t gemm_tc_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& w,
-                           const uint8_t* repacked, int K, int N, int bs, void* Y) {
+namespace {
+
+cudaError_t launch_tc_impl(LaunchCtx& ctx, const void* A, int M, const QWeight& w, const uint8_t* repacked, int K,
+                           int N, int bs, void* Y, int Mout, float* Yf, const float* biasf, const int* rexp) {
   if (K % 16 != 0) return cudaErrorNotSupported;
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
@@ -444,12 +470,31 @@ cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& 
   a.status = ctx.status;
   a.bias = static_cast<const __half*>(ctx.bias);
   a.bias_mode = ctx.bias_mode;
+  a.Mout = Mout;
+  a.Yf = Yf;
+  a.biasf = biasf;
+  a.rexp = rexp;
   const int tiles = a.mtiles * a.ntiles;
   const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const bool f32 = Yf != nullptr;
+  auto kern = f32 ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  ctx.variant = "gemm_tcgen05_w128xa256";
-  return launch_kernel(ctx, gemm_tc_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, a, tmap);
+  ctx.variant = f32 ? "gemm_tcgen05_w128xa256_f32split" : "gemm_tcgen05_w128xa256";
+  return launch_kernel(ctx, kern, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, a, tmap);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& w,
+                           const uint8_t* repacked, int K, int N, int bs, void* Y) {
+  return launch_tc_impl(ctx, A, M, w, repacked, K, N, bs, Y, M, nullptr, nullptr, nullptr);
+}
+
+cudaError_t launch_gemm_tc_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w,
+                                    const uint8_t* repacked, int K, int N, int bs, float* Y, const float* bias,
+                                    const int* rexp) {
+  return launch_tc_impl(ctx, A2, 2 * M, w, repacked, K, N, bs, nullptr, M, Y, bias, rexp);
 }
 
 }  // namespace mnb

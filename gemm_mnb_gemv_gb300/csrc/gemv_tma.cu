@@ -46,6 +46,10 @@ struct TmaGemvArgs {
   uint32_t* status;
   const __half* bias;
   int bias_mode;
+  // fp32 activations (AF): A, Y and bias are fp32; Y = acc + bias with no rounding.
+  const float* Af;
+  float* Yf;
+  const float* biasf;
 };
 
 __device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
@@ -61,7 +65,22 @@ __device__ __forceinline__ float dot_word_tma(uint32_t w, uint32_t zlo, uint32_t
   return acc;
 }
 
-template <int NCW, int WG, int CPS, int VPG, bool BS16, bool PAIR, bool S16, bool ZP>
+// fp32 activations: the exact fp16 (code - zp) pairs widen to fp32 and multiply fp32
+// activations a8[0..7] (word order: nibble i pairs with a8[i], nibble i + 4 with a8[i + 4]).
+__device__ __forceinline__ float dot_word_f32(uint32_t w, uint32_t zlo, uint32_t zhi, const float* a8,
+                                              float acc) {
+  uint32_t d[4];
+  nibbles_to_centered_half2(w, zlo, zhi, d);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&d[i]);
+    acc = fmaf(__low2float(h), a8[i], acc);
+    acc = fmaf(__high2float(h), a8[i + 4], acc);
+  }
+  return acc;
+}
+
+template <int NCW, int WG, int CPS, int VPG, bool BS16, bool PAIR, bool S16, bool ZP, bool AF = false>
 __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
     gemv_tma_kernel(const TmaGemvArgs p) {
   constexpr int kThreads = (NCW + 1) * 32;
@@ -148,6 +167,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
     // Per owned chunk: activations (paired) and byte offsets, inside one column's
     // regions, of its weights, its (first) scale and its zero-point byte.
     uint32_t a[CPS][16];
+    float af[AF ? CPS : 1][AF ? 32 : 1];
     uint32_t wofs[CPS], sofs[CPS], zofs[CPS], zsh[CPS];
     bool cval[CPS];
 #pragma unroll
@@ -159,11 +179,23 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
       sofs[j] = (uint32_t)gi * kSB;
       zofs[j] = BS16 ? (uint32_t)c : (uint32_t)(gi >> 1);
       zsh[j] = BS16 ? 0u : (uint32_t)((gi & 1) * 4);
+      if constexpr (AF) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if (cval[j]) x = *reinterpret_cast<const uint4*>(p.A + (long long)c * 32 + q * 8);
-        pair_halves_stride4(x, &a[j][q * 4]);
+        for (int q = 0; q < 8; ++q) {
+          float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (cval[j]) x = *reinterpret_cast<const float4*>(p.Af + (long long)c * 32 + q * 4);
+          af[j][4 * q] = x.x;
+          af[j][4 * q + 1] = x.y;
+          af[j][4 * q + 2] = x.z;
+          af[j][4 * q + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (cval[j]) x = *reinterpret_cast<const uint4*>(p.A + (long long)c * 32 + q * 8);
+          pair_halves_stride4(x, &a[j][q * 4]);
+        }
       }
     }
     const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
@@ -201,10 +233,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
                 const uint32_t z0 = zb & 15u, z1 = zb >> 4;
                 const uint32_t zl0 = ZP ? zp_lo_const(z0) : zl8, zh0 = ZP ? zp_hi_const(z0) : zh8;
                 const uint32_t zl1 = ZP ? zp_lo_const(z1) : zl8, zh1 = ZP ? zp_hi_const(z1) : zh8;
-                float p0 = dot_word_tma(w4.x, zl0, zh0, &a[j][0], 0.0f);
-                p0 = dot_word_tma(w4.y, zl0, zh0, &a[j][4], p0);
-                float p1 = dot_word_tma(w4.z, zl1, zh1, &a[j][8], 0.0f);
-                p1 = dot_word_tma(w4.w, zl1, zh1, &a[j][12], p1);
+                float p0, p1;
+                if constexpr (AF) {
+                  p0 = dot_word_f32(w4.x, zl0, zh0, &af[j][0], 0.0f);
+                  p0 = dot_word_f32(w4.y, zl0, zh0, &af[j][8], p0);
+                  p1 = dot_word_f32(w4.z, zl1, zh1, &af[j][16], 0.0f);
+                  p1 = dot_word_f32(w4.w, zl1, zh1, &af[j][24], p1);
+                } else {
+                  p0 = dot_word_tma(w4.x, zl0, zh0, &a[j][0], 0.0f);
+                  p0 = dot_word_tma(w4.y, zl0, zh0, &a[j][4], p0);
+                  p1 = dot_word_tma(w4.z, zl1, zh1, &a[j][8], 0.0f);
+                  p1 = dot_word_tma(w4.w, zl1, zh1, &a[j][12], p1);
+                }
                 float s0, s1;
                 if (S16) {
                   const uint32_t sh = lds_u32_a(cs + sofs[j]);
@@ -220,10 +260,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
               } else {
                 const uint32_t zz = (zb >> zsh[j]) & 15u;
                 const uint32_t zlo = ZP ? zp_lo_const(zz) : zl8, zhi = ZP ? zp_hi_const(zz) : zh8;
-                float q0 = dot_word_tma(w4.x, zlo, zhi, &a[j][0], 0.0f);
-                float q1 = dot_word_tma(w4.y, zlo, zhi, &a[j][4], 0.0f);
-                q0 = dot_word_tma(w4.z, zlo, zhi, &a[j][8], q0);
-                q1 = dot_word_tma(w4.w, zlo, zhi, &a[j][12], q1);
+                float q0, q1;
+                if constexpr (AF) {
+                  q0 = dot_word_f32(w4.x, zlo, zhi, &af[j][0], 0.0f);
+                  q1 = dot_word_f32(w4.y, zlo, zhi, &af[j][8], 0.0f);
+                  q0 = dot_word_f32(w4.z, zlo, zhi, &af[j][16], q0);
+                  q1 = dot_word_f32(w4.w, zlo, zhi, &af[j][24], q1);
+                } else {
+                  q0 = dot_word_tma(w4.x, zlo, zhi, &a[j][0], 0.0f);
+                  q1 = dot_word_tma(w4.y, zlo, zhi, &a[j][4], 0.0f);
+                  q0 = dot_word_tma(w4.z, zlo, zhi, &a[j][8], q0);
+                  q1 = dot_word_tma(w4.w, zlo, zhi, &a[j][12], q1);
+                }
                 const float s = S16 ? half_bits_to_float(lds_u16_a(cs + sofs[j]))
                                     : __uint_as_float(lds_u32_a(cs + sofs[j]));
                 acc = fmaf(q0 + q1, s, acc);
@@ -260,11 +308,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
       for (int w = 0; w < WG; ++w) s += red[w][t][c];
       v[t] = s;
     }
-    __half out;
-    if (PAIR) out = __float2half_rn(silu_f32(v[0]) * v[NWT - 1]);
-    else out = round_out(v[0], p.bias, n0 + c, p.bias_mode);
-    if (bad) out = __ushort_as_half(0x7e00);
-    reinterpret_cast<__half*>(p.Y)[n0 + c] = out;
+    if constexpr (AF) {
+      float out = v[0] + (p.biasf ? p.biasf[n0 + c] : 0.0f);
+      if (bad) out = __uint_as_float(0x7fc00000u);
+      p.Yf[n0 + c] = out;
+    } else {
+      __half out;
+      if (PAIR) out = __float2half_rn(silu_f32(v[0]) * v[NWT - 1]);
+      else out = round_out(v[0], p.bias, n0 + c, p.bias_mode);
+      if (bad) out = __ushort_as_half(0x7e00);
+      reinterpret_cast<__half*>(p.Y)[n0 + c] = out;
+    }
   }
 }
 
@@ -291,8 +345,27 @@ TmaKernel pick(bool bs16, bool s16, bool zp) {
 #undef MNB_PICK
 }
 
+// fp32 activations (single weight, at most two chunks per lane so the fp32 activations
+// stay in registers).
+template <int WG, int CPS>
+TmaKernel pick_af(bool bs16, bool s16, bool zp) {
+#define MNB_PICK(B, S, Z) gemv_tma_kernel<kNCW, WG, CPS, 4, B, false, S, Z, true>
+  if (bs16) {
+    if (s16) return zp ? MNB_PICK(true, true, true) : MNB_PICK(true, true, false);
+    return zp ? MNB_PICK(true, false, true) : MNB_PICK(true, false, false);
+  }
+  if (s16) return zp ? MNB_PICK(false, true, true) : MNB_PICK(false, true, false);
+  return zp ? MNB_PICK(false, false, true) : MNB_PICK(false, false, false);
+#undef MNB_PICK
+}
+
 template <bool PAIR>
-TmaKernel select_kernel(int wg, int cps, bool bs16, bool s16, bool zp) {
+TmaKernel select_kernel(int wg, int cps, bool bs16, bool s16, bool zp, bool af) {
+  if (af) {
+    if (wg == 4) return pick_af<4, 1>(bs16, s16, zp);
+    if (cps == 1) return pick_af<8, 1>(bs16, s16, zp);
+    return pick_af<8, 2>(bs16, s16, zp);
+  }
   if (wg == 4) return pick<4, 1, PAIR>(bs16, s16, zp);
   if (cps == 1) return pick<8, 1, PAIR>(bs16, s16, zp);
   if (cps == 2) return pick<8, 2, PAIR>(bs16, s16, zp);
@@ -301,8 +374,10 @@ TmaKernel select_kernel(int wg, int cps, bool bs16, bool s16, bool zp) {
 
 template <bool PAIR>
 cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int K, int N, int bs,
-                            void* Y) {
+                            void* Y, const float* Af = nullptr, float* Yf = nullptr,
+                            const float* biasf = nullptr) {
   constexpr int NWT = PAIR ? 2 : 1;
+  const bool af = Af != nullptr;
   if (K % 32 != 0) return cudaErrorNotSupported;
   if (PAIR && (w[0].scales_f16 != w[1].scales_f16 || (w[0].zp == nullptr) != (w[1].zp == nullptr)))
     return cudaErrorNotSupported;
@@ -317,7 +392,7 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
     wg = 8;
     cps = (C + 255) / 256;
     if (cps == 3) cps = 4;
-    if (cps > 4) return cudaErrorNotSupported;
+    if (cps > 4 || (af && cps > 2)) return cudaErrorNotSupported;
   }
   const int ng = kNCW / wg;
   const int cb = ng * (PAIR ? 2 : 4);
@@ -349,15 +424,18 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   a.status = ctx.status;
   a.bias = static_cast<const __half*>(ctx.bias);
   a.bias_mode = PAIR ? 0 : ctx.bias_mode;
+  a.Af = Af;
+  a.Yf = Yf;
+  a.biasf = biasf;
   int grid = ctx.num_sms;
   if (grid > N) grid = N;
   const int min_grid = (N + kMaxColsPerCta - 1) / kMaxColsPerCta;
   if (grid < min_grid) grid = min_grid;
   const size_t smem = (size_t)a.stages * a.stage_bytes;
-  auto kern = select_kernel<PAIR>(wg, cps, bs == 16, s16, zp);
+  auto kern = select_kernel<PAIR>(wg, cps, bs == 16, s16, zp, af);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ctx.variant = PAIR ? "gemv_pair_swiglu_tma_ring" : "gemv_tma_ring";
+  ctx.variant = PAIR ? "gemv_pair_swiglu_tma_ring" : (af ? "gemv_f32_tma_ring" : "gemv_tma_ring");
   return launch_kernel(ctx, kern, dim3(grid), dim3((kNCW + 1) * 32), smem, a);
 }
 
@@ -372,6 +450,11 @@ cudaError_t launch_gemv_pair_swiglu_tma(LaunchCtx& ctx, const void* A, const QWe
                                         const QWeight& up, int K, int N, int bs, void* out) {
   const QWeight w[2] = {gate, up};
   return launch_tma_impl<true>(ctx, A, w, K, N, bs, out);
+}
+
+cudaError_t launch_gemv_f32_tma(LaunchCtx& ctx, const float* A, const QWeight& w, int K, int N, int bs,
+                                float* Y, const float* bias) {
+  return launch_tma_impl<false>(ctx, nullptr, &w, K, N, bs, nullptr, A, Y, bias);
 }
 
 }  // namespace mnb

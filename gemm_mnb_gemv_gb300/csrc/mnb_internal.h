@@ -52,6 +52,20 @@ cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeig
 // M > 16 on the tcgen05 tensor cores, reading the repacked operand.
 cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& w,
                            const uint8_t* repacked, int K, int N, int bs, void* Y);
+// fp32 activations.  M = 1: bulk-copy GEMV with fp32 activations (K <= 16384).  M >= 2:
+// rows split into fp16 hi/lo pairs (A2 holds 2M rows, rexp M exponents), then the small-M
+// kernel (2M <= 16) or the tcgen05 kernel with the pair-summing fp32 epilogue.  The generic
+// fp32 kernel takes any shape.
+cudaError_t launch_gemv_f32_tma(LaunchCtx& ctx, const float* A, const QWeight& w, int K, int N, int bs,
+                                float* Y, const float* bias);
+cudaError_t launch_split_f32(LaunchCtx& ctx, const float* A, int M, int K, void* A2, int* rexp);
+cudaError_t launch_gemm_smallm_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w, int K, int N,
+                                        int bs, float* Y, const float* bias, const int* rexp);
+cudaError_t launch_gemm_tc_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w,
+                                    const uint8_t* repacked, int K, int N, int bs, float* Y, const float* bias,
+                                    const int* rexp);
+cudaError_t launch_generic_f32(LaunchCtx& ctx, const float* A, int M, const QWeight& w, int K, int N, int bs,
+                               float* Y, const float* bias);
 // Any M, any K % 16 == 0: CUDA-core kernel, fp32 arithmetic.
 cudaError_t launch_generic(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N,
                            int bs, void* Y);

@@ -21,7 +21,8 @@
  *   - Every pointer argument is device memory owned by the caller (except where an
  *     argument is marked HOST); the library keeps no reference after the call returns
  *     and allocates nothing.
- *   - A and Y are fp16 (IEEE binary16, passed as raw 16-bit storage), row-major.
+ *   - A and Y are fp16 (IEEE binary16, passed as raw 16-bit storage), row-major, except
+ *     in mnb_gemm_f32, where they are fp32.
  *   - Every device pointer must be non-NULL (except zero_points, workspace when
  *     ws_bytes is 0, and repacked where stated) and 16-byte aligned:
  *     otherwise MNB_ERR_INVALID_ARG / MNB_ERR_MISALIGNED.
@@ -164,6 +165,36 @@ MNB_API mnb_status mnb_gemm_bias(const void *A, int M, mnb_weight w, const uint8
  */
 MNB_API mnb_status mnb_gemv_gate_up_swiglu(const void *A, mnb_weight gate, mnb_weight up, int K, int N,
                                    int block_size, void *out, mnb_stream stream);
+
+/*
+ * ---- fp32 activations ----
+ *
+ * The operator's fp32 path (matmul_nbits.rs, MatMulNBitsKernel::run with a Float32 A:
+ * matmul_nbits_gemv_f32 for M = 1, dequantise-then-GEMM otherwise): A [M, K], Y [M, N]
+ * and the optional bias [N] are fp32 (row-major, 16-byte aligned), Y = A . dequant(B)^T
+ * + bias with no fp16 rounding anywhere. M = 1 multiplies fp32 activations directly. For
+ * M >= 2 every row of A is scaled by a power of two and split into two fp16 rows (high
+ * and low part, together within 2^-22 of the row) that the fp16 tensor-core kernels
+ * multiply; their two accumulators are added and scaled back in fp32. Either way the
+ * weights are exact and the accumulation is fp32, so |Y - exact| <= 2e-3 * sum_k |a_k
+ * w_nk| + 1e-5 holds with a wide margin. A row holding inf or NaN gives non-finite
+ * outputs in that row.
+ */
+
+/* Workspace bytes mnb_gemm_f32 needs: 0 for M = 1, else 4*M*K + 4*M rounded up to 16. */
+MNB_API size_t mnb_workspace_bytes_f32(int M, int K, int N, int block_size);
+
+/*
+ * fp32 Y[M, N] = A[M, K] . dequant(B)^T (+ bias[n] when bias is not NULL). Weight
+ * arguments as mnb_gemm; `repacked` (mnb_repack) is required when M > 8, because the
+ * split activation then has more than 16 rows and runs on the tcgen05 kernel. The
+ * workspace holds the split activation and the row exponents; its contents need no
+ * initialisation and are overwritten by each call, so calls sharing one workspace must
+ * be ordered on one stream.
+ */
+MNB_API mnb_status mnb_gemm_f32(const float *A, int M, mnb_weight w, const uint8_t *repacked, int K, int N,
+                                int block_size, const float *bias, void *workspace, size_t ws_bytes, float *Y,
+                                mnb_stream stream);
 
 /*
  * ---- Act-order weights (g_idx) ----

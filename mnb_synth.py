@@ -111,6 +111,30 @@ def make_activation(wl: Workload, tag: str = "A", rows: int | None = None) -> np
     return x.astype(np.float16).reshape(rows, wl.K)
 
 
+def make_activation_f32(wl: Workload, tag: str = "A", rows: int | None = None, recipe: str | None = None):
+    """fp32 activations ``[rows or M, K]`` (not rounded to fp16).
+
+    ``recipe`` defaults to the workload's; ``"wide"`` draws magnitudes log-uniform over
+    1e-6 .. 1e6 with random signs (values far outside the fp16 range).
+    """
+    rows = wl.M if rows is None else rows
+    recipe = wl.act if recipe is None else recipe
+    seed = fnv1a64(f"{wl.name}/{tag}/f32")
+    n = rows * wl.K
+    if recipe == "wide":
+        u = uniform01(seed, 2 * n)
+        x = np.where(u[0::2] < 0.5, -1.0, 1.0) * 10.0 ** (12.0 * u[1::2] - 6.0)
+    elif recipe == "uniform1":
+        x = uniform01(seed, n) * 2.0 - 1.0
+    elif recipe == "normal":
+        x = normal(seed, n)
+    elif recipe == "normal_clip4":
+        x = np.clip(normal(seed, n), -4.0, 4.0)
+    else:
+        raise ValueError(recipe)
+    return x.astype(np.float32).reshape(rows, wl.K)
+
+
 @dataclasses.dataclass
 class QuantWeight:
     """Host copy of one quantised weight in MatMulNBits storage."""

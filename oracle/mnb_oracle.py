@@ -169,9 +169,13 @@ def dequant_kn_f32(packed, scales, zp, K: int, N: int, block_size: int, g_idx=No
 
 
 def activations_f64(A: np.ndarray) -> np.ndarray:
-    if A.dtype != np.float16:
-        raise TypeError("activations are fp16")
-    return f16_to_f64(A).reshape(A.shape)
+    """Exact fp64 value of fp16 activations (decoded from their bits) or fp32 ones
+    (the operator's fp32 path, matmul_nbits.rs: A of type Float32, widened exactly)."""
+    if A.dtype == np.float16:
+        return f16_to_f64(A).reshape(A.shape)
+    if A.dtype == np.float32:
+        return A.astype(np.float64)
+    raise TypeError(f"activations are fp16 or fp32, got {A.dtype}")
 
 
 def matmul(A, packed, scales, zp, K: int, N: int, block_size: int, g_idx=None):

@@ -10,6 +10,8 @@
 * fp16 decoding against numpy's own conversion for all 65536 bit patterns,
 * silu against ``x * scipy.special.expit(x)``,
 * the repacked layout: a hand-placed code, and the round trip,
+* fp32 activations are taken at their exact value (rational brute force with values
+  that fp16 cannot hold),
 * act-order ``g_idx``: the identity reduces to the plain layout; a weight built the
   act-order way (codes quantised in a visit order, stored in k order) dequantises to
   the same matrix; exact rational brute force with uneven and out-of-range groups;
@@ -437,3 +439,29 @@ def test_act_order_product_equivalence_exact():
     Y2, _ = orc.matmul(Ag, pk, sc, zpp, Kp, N, bs)
     np.testing.assert_array_equal(Y2, Y)
     assert np.all(Ag[:, perm < 0] == 0) and not np.any(np.signbit(Ag[:, perm < 0]))
+
+
+def test_f32_activations_exact_rational():
+    """fp32 activations enter at their own value, not rounded to fp16: 1 + 2^-20, 1e6 and
+    3e-9 are not fp16 numbers, and the product equals the exact rational sum."""
+    K, N, bs = 32, 2, 16
+    rng = np.random.default_rng(3)
+    codes_nk = rng.integers(0, 16, size=(N, K))
+    packed = _pack_codes(codes_nk)
+    zp = _pack_zp(rng.integers(0, 16, size=(N, K // bs)))
+    scales = np.array([[0.25, 0.125], [0.5, 2.0]], dtype=np.float32)
+    A = np.full((1, K), 1.0 + 2.0 ** -20, dtype=np.float32)
+    A[0, 3], A[0, 17] = 1e6, 3e-9
+    Y, _ = orc.matmul(A, packed, scales, zp, K, N, bs)
+    zpn = orc.zero_points(zp, K, N, bs)
+    for n in range(N):
+        acc = fractions.Fraction(0)
+        for k in range(K):
+            acc += fractions.Fraction(float(A[0, k])) * int(codes_nk[n, k] - zpn[n, k // bs]) * \
+                fractions.Fraction(float(scales[n, k // bs]))
+        assert abs(Y[0, n] - float(acc)) <= 1e-12 * abs(float(acc)) + 1e-300
+    # within the fp16 range, the fp16-rounded activation gives a different result
+    A[0, 3] = 1.0
+    Y32, _ = orc.matmul(A, packed, scales, zp, K, N, bs)
+    Y16, _ = orc.matmul(A.astype(np.float16), packed, scales, zp, K, N, bs)
+    assert not np.allclose(Y16, Y32, rtol=1e-9, atol=0)
