@@ -33,3 +33,8 @@ def assert_within_bound(y_gpu, Y_ref, B, what=""):
             f"{what}: {int(bad.sum())} of {bad.size} outside the bound; worst at {i}: "
             f"gpu {y[i]!r} ref {Y_ref[i]!r} err {err[i]:.3e} tol {tol[i]:.3e}")
     return float(np.max(err / tol))
+
+
+def tc_variant(N: int, f32: bool = False) -> str:
+    """Name of the tensor-core kernel the dispatcher picks for M > 16 (fp32: M > 8)."""
+    return "gemm_tcgen05_w128xa256" + ("_f32split" if f32 else "")

@@ -14,7 +14,7 @@ import pytest
 
 import mnb_synth as syn
 from oracle import mnb_oracle as orc
-from tests.helpers import assert_within_bound, upload_act, upload_weight
+from tests.helpers import assert_within_bound, tc_variant, upload_act, upload_weight
 
 pytestmark = pytest.mark.gpu
 
@@ -143,7 +143,7 @@ def test_gemm_act_order_parity(env, name, M, K, N, bs, sdt, zp, kind):
     variant = mnb.mnb_last_variant()
     assert variant != "act_order_gather", variant  # the product kernel's name is reported
     if M > 16:
-        assert variant == "gemm_tcgen05_w128xa256", variant
+        assert variant == tc_variant(N), variant
     mnb.mnb_check_device_status()
 
 

@@ -52,6 +52,7 @@ F32_CASES = [
     ("f32_m9", 9, 1024, 256, 64, "f16", True, "normal", True, "gemm_tcgen05_w128xa256_f32split"),
     ("f32_m40_wide", 40, 2048, 384, 128, "f32", True, "wide", False, "gemm_tcgen05_w128xa256_f32split"),
     ("f32_m300", 300, 1024, 200, 32, "f16", False, "normal", True, "gemm_tcgen05_w128xa256_f32split"),
+    ("f32_m33_n96", 33, 512, 96, 32, "f16", True, "normal", True, "gemm_tcgen05_w128xa256_f32split"),
 ]
 
 

@@ -13,7 +13,7 @@ import pytest
 
 import mnb_synth as syn
 from oracle import mnb_oracle as orc
-from tests.helpers import assert_within_bound, upload_act, upload_weight
+from tests.helpers import assert_within_bound, tc_variant, upload_act, upload_weight
 
 pytestmark = pytest.mark.gpu
 
@@ -187,7 +187,7 @@ def test_gemm_large_m_ragged(env, M, K, N, bs, sdt, zp):
     packed, scales, zpt = upload_weight(w, dev)
     rp = mnb.mnb_repack(packed, K, N, bs)
     y = mnb.mnb_gemm(upload_act(A, dev), packed, scales, zpt, K, N, bs, repacked=rp)
-    assert mnb.mnb_last_variant() == "gemm_tcgen05_w128xa256"
+    assert mnb.mnb_last_variant() == tc_variant(N)
     torch.cuda.synchronize()
     mnb.mnb_check_device_status()
     Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
@@ -416,6 +416,7 @@ BIAS_CASES = [  # (M, K, N, bs, expected variant prefix)
     (4, 4096, 300, 64, "gemm_smallm"),
     (3, 96, 77, 16, "generic"),
     (64, 256, 300, 128, "gemm_tcgen05"),
+    (40, 256, 100, 64, "gemm_tcgen05"),
 ]
 
 
