@@ -149,15 +149,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
     pdl_wait();
     // Stage the activations once: entry (set s, chunk c, lane l = 4g + t) holds
     // A[8s + g][32c + 8t .. +8], paired (x0,x4)(x1,x5)(x2,x6)(x3,x7).
+    // Eight loads in flight per thread before any is used, so the L2 latency is paid once
+    // per batch rather than once per entry.
     const int entries = MSETS * C * 32;
-    for (int e = tid; e < entries; e += kCW * 32) {
-      const int l = e & 31, c = (e >> 5) % C, s = (e >> 5) / C;
-      const int m = 8 * s + (l >> 2), k = 32 * c + 8 * (l & 3);
-      uint4 x = make_uint4(0, 0, 0, 0);
-      if (m < p.M) x = *reinterpret_cast<const uint4*>(p.A + (long long)m * p.K + k);
-      uint32_t q[4];
-      pair_halves_stride4(x, q);
-      *reinterpret_cast<uint4*>(xs + (size_t)e * 16) = make_uint4(q[0], q[1], q[2], q[3]);
+    constexpr int kBatch = 8;
+    for (int e0 = tid; e0 < entries; e0 += kBatch * kCW * 32) {
+      uint4 x[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * kCW * 32;
+        const int l = e & 31, c = (e >> 5) % C, s = (e >> 5) / C;
+        const int m = 8 * s + (l >> 2), k = 32 * c + 8 * (l & 3);
+        x[u] = make_uint4(0, 0, 0, 0);
+        if (e < entries && m < p.M) x[u] = *reinterpret_cast<const uint4*>(p.A + (long long)m * p.K + k);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * kCW * 32;
+        if (e < entries) {
+          uint32_t q[4];
+          pair_halves_stride4(x[u], q);
+          *reinterpret_cast<uint4*>(xs + (size_t)e * 16) = make_uint4(q[0], q[1], q[2], q[3]);
+        }
+      }
     }
     consumer_bar();
 
