@@ -291,11 +291,14 @@ class DeviceBench:
                 mnb.mnb_gemm_act_order(A, *copies[i % ncopy], perm_d, wl.K, kp, wl.N, wl.block_size,
                                        workspace=ws, out=Y)
 
-        ms, _ = self.time_graph(rec, 2 * calls, steps, warmup, sampler)
+        # M = 1 (K' <= 8192): one launch per call, the GEMV gathers its own activations;
+        # otherwise a gather pass and the block kernel.
+        ms, _ = self.time_graph(rec, calls if wl.M == 1 else 2 * calls, steps, warmup, sampler)
         us = ms * 1e3 / calls
+        variant = mnb.mnb_last_variant()
         return {"workload": f"{wl.name}_{kind}", "K_prepared": kp, "us_per_call": us,
                 "gbps": call_bytes(wl) / (us * 1e3), "copies": ncopy,
-                "variant": "act_order_gather + " + mnb.mnb_last_variant()}
+                "variant": variant if variant.endswith("_gather") else "act_order_gather + " + variant}
 
     def gemm(self, wl, steps, warmup, sampler, calls, repacked: bool):
         torch, mnb = self.torch, self.mnb

@@ -499,11 +499,14 @@ mnb_status mnb_gemm_act_order(const void* A, int M, mnb_weight w, const uint8_t*
   if ((st = check_ptr(fn, "workspace", workspace)) != MNB_OK) return st;
   mnb::LaunchCtx ctx;
   if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
-  cudaError_t e = mnb::launch_act_order_gather(ctx, A, M, K, perm, K_prepared, workspace);
-  if (e == cudaSuccess) {
-    ctx.bias = bias_mode ? bias : nullptr;
-    ctx.bias_mode = bias_mode;
-    e = dispatch_gemm(ctx, workspace, M, q, repacked, K_prepared, N, block_size, Y);
+  ctx.bias = bias_mode ? bias : nullptr;
+  ctx.bias_mode = bias_mode;
+  // M = 1: the GEMV gathers its activations itself (no second launch, workspace unused).
+  cudaError_t e = M == 1 ? mnb::launch_gemv_tma_gather(ctx, A, perm, K, q, K_prepared, N, block_size, Y)
+                         : cudaErrorNotSupported;
+  if (e == cudaErrorNotSupported) {
+    e = mnb::launch_act_order_gather(ctx, A, M, K, perm, K_prepared, workspace);
+    if (e == cudaSuccess) e = dispatch_gemm(ctx, workspace, M, q, repacked, K_prepared, N, block_size, Y);
   }
   return finish(fn, e, ctx);
 }
@@ -576,13 +579,16 @@ mnb_status mnb_gemm_act_order_noalloc(const void* A, int M, mnb_weight w, const 
   if ((st = noalloc_scratch(fn, &scratch)) != MNB_OK) return st;
   mnb::LaunchCtx ctx;
   if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
-  // The gather writes every byte of A'[M, K'] that the product then reads, padding
-  // slots included, so nothing left in the array by an earlier call is used.
-  cudaError_t e = mnb::launch_act_order_gather(ctx, A, M, K, perm, K_prepared, scratch);
-  if (e == cudaSuccess) {
-    ctx.bias = bias_mode ? bias : nullptr;
-    ctx.bias_mode = bias_mode;
-    e = dispatch_gemm(ctx, scratch, M, q, repacked, K_prepared, N, block_size, Y);
+  // When the gather pass runs (M > 1, or K' beyond the fused GEMV) it writes every byte
+  // of A'[M, K'] that the product then reads, padding slots included, so nothing left in
+  // the array by an earlier call is used.
+  ctx.bias = bias_mode ? bias : nullptr;
+  ctx.bias_mode = bias_mode;
+  cudaError_t e = M == 1 ? mnb::launch_gemv_tma_gather(ctx, A, perm, K, q, K_prepared, N, block_size, Y)
+                         : cudaErrorNotSupported;
+  if (e == cudaErrorNotSupported) {
+    e = mnb::launch_act_order_gather(ctx, A, M, K, perm, K_prepared, scratch);
+    if (e == cudaSuccess) e = dispatch_gemm(ctx, scratch, M, q, repacked, K_prepared, N, block_size, Y);
   }
   return finish(fn, e, ctx);
 }

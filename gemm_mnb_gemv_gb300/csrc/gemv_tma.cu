@@ -50,6 +50,9 @@ struct TmaGemvArgs {
   const float* Af;
   float* Yf;
   const float* biasf;
+  // Act-order gather (GA): activation k' is A[perm[k']] (0 where perm = -1), A of Ka halves.
+  const int32_t* perm;
+  int Ka;
 };
 
 __device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
@@ -80,7 +83,8 @@ __device__ __forceinline__ float dot_word_f32(uint32_t w, uint32_t zlo, uint32_t
   return acc;
 }
 
-template <int NCW, int WG, int CPS, int VPG, bool BS16, bool PAIR, bool S16, bool ZP, bool AF = false>
+template <int NCW, int WG, int CPS, int VPG, bool BS16, bool PAIR, bool S16, bool ZP, bool AF = false,
+          bool GA = false>
 __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
     gemv_tma_kernel(const TmaGemvArgs p) {
   constexpr int kThreads = (NCW + 1) * 32;
@@ -160,9 +164,53 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
   } else {
     // ------------------------------- consumers ------------------------------------
     pdl_launch_dependents();
-    pdl_wait();
     const int g = warp / WG, wig = warp % WG;
     const int ls = wig * 32 + lane;
+    // Act-order gather: consumer thread i places A'[k'] = A[perm[k']] for k' = i, i + 512,
+    // ... (at most kGaPer of them).  perm is constant for the weight, so its entries are
+    // loaded before the wait; A only after it.
+    constexpr int kGaPer = 8192 / (NCW * 32);
+    int pidx[GA ? kGaPer : 1];
+    if constexpr (GA) {
+      static_assert(CPS == 1, "the gathering GEMV keeps one chunk per lane");
+#pragma unroll
+      for (int u = 0; u < kGaPer; ++u) {
+        const int kp = tid + u * NCW * 32;
+        pidx[u] = kp < p.K ? __ldg(p.perm + kp) : -1;
+      }
+    }
+    pdl_wait();
+    // Act-order gather, in shared memory behind the ring: copy A (Ka halves) with 16-byte
+    // loads, permute it into A' (K' halves), then every lane loads its chunk of A' as usual.
+    const uint32_t a_u32 = smem_u32(ring) + (uint32_t)(p.stages * p.stage_bytes);
+    const uint32_t a2_u32 = a_u32 + (uint32_t)(((p.Ka * 2 + 15) >> 4) << 4);
+    if constexpr (GA) {
+      for (int i = tid; i < (p.Ka >> 3); i += NCW * 32) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p.A + 8 * i);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a_u32 + 16u * (uint32_t)i), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
+      bool bad = false;
+#pragma unroll
+      for (int u = 0; u < kGaPer; ++u) {
+        const int kp = tid + u * NCW * 32;
+        if (kp < p.K) {
+          const int src = pidx[u];
+          uint32_t h = 0u;
+          if (src >= 0 && src < p.Ka) {
+            h = lds_u16_a(a_u32 + 2u * (uint32_t)src);
+          } else if (src != -1) {
+            bad = true;
+          }
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(a2_u32 + 2u * (uint32_t)kp), "h"((unsigned short)h)
+                       : "memory");
+        }
+      }
+      if (bad) report_status(p.status, kStatusBadIndex);
+      asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
+    }
 
     // Per owned chunk: activations (paired) and byte offsets, inside one column's
     // regions, of its weights, its (first) scale and its zero-point byte.
@@ -188,6 +236,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
           af[j][4 * q + 1] = x.y;
           af[j][4 * q + 2] = x.z;
           af[j][4 * q + 3] = x.w;
+        }
+      } else if constexpr (GA) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (cval[j]) x = lds128_a(a2_u32 + (uint32_t)c * 64u + (uint32_t)q * 16u);
+          pair_halves_stride4(x, &a[j][q * 4]);
         }
       } else {
 #pragma unroll
@@ -359,8 +414,22 @@ TmaKernel pick_af(bool bs16, bool s16, bool zp) {
 #undef MNB_PICK
 }
 
+// Act-order gather (single weight, one chunk per lane).
+template <int WG>
+TmaKernel pick_ga(bool bs16, bool s16, bool zp) {
+#define MNB_PICK(B, S, Z) gemv_tma_kernel<kNCW, WG, 1, 4, B, false, S, Z, false, true>
+  if (bs16) {
+    if (s16) return zp ? MNB_PICK(true, true, true) : MNB_PICK(true, true, false);
+    return zp ? MNB_PICK(true, false, true) : MNB_PICK(true, false, false);
+  }
+  if (s16) return zp ? MNB_PICK(false, true, true) : MNB_PICK(false, true, false);
+  return zp ? MNB_PICK(false, false, true) : MNB_PICK(false, false, false);
+#undef MNB_PICK
+}
+
 template <bool PAIR>
-TmaKernel select_kernel(int wg, int cps, bool bs16, bool s16, bool zp, bool af) {
+TmaKernel select_kernel(int wg, int cps, bool bs16, bool s16, bool zp, bool af, bool ga) {
+  if (ga) return wg == 4 ? pick_ga<4>(bs16, s16, zp) : pick_ga<8>(bs16, s16, zp);
   if (af) {
     if (wg == 4) return pick_af<4, 1>(bs16, s16, zp);
     if (cps == 1) return pick_af<8, 1>(bs16, s16, zp);
@@ -375,9 +444,10 @@ TmaKernel select_kernel(int wg, int cps, bool bs16, bool s16, bool zp, bool af) 
 template <bool PAIR>
 cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int K, int N, int bs,
                             void* Y, const float* Af = nullptr, float* Yf = nullptr,
-                            const float* biasf = nullptr) {
+                            const float* biasf = nullptr, const int32_t* perm = nullptr, int Ka = 0) {
   constexpr int NWT = PAIR ? 2 : 1;
   const bool af = Af != nullptr;
+  const bool ga = perm != nullptr;
   if (K % 32 != 0) return cudaErrorNotSupported;
   if (PAIR && (w[0].scales_f16 != w[1].scales_f16 || (w[0].zp == nullptr) != (w[1].zp == nullptr)))
     return cudaErrorNotSupported;
@@ -394,6 +464,7 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
     if (cps == 3) cps = 4;
     if (cps > 4 || (af && cps > 2)) return cudaErrorNotSupported;
   }
+  if (ga && cps != 1) return cudaErrorNotSupported;
   const int ng = kNCW / wg;
   const int cb = ng * (PAIR ? 2 : 4);
   const int G = K / bs;
@@ -418,8 +489,11 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
     a.zp[t] = q.zp;
   }
   a.stage_bytes = cb * NWT * (a.row_bytes + a.sbytes + a.zbytes);
-  if (a.stage_bytes * 2 > kRingBudget) return cudaErrorNotSupported;
-  a.stages = kRingBudget / a.stage_bytes;
+  // Shared copies of A and of the permuted A' for the gather.
+  const int abytes = ga ? (Ka * 2 + 15) / 16 * 16 + K * 2 : 0;
+  const int ring_budget = kRingBudget - abytes;
+  if (a.stage_bytes * 2 > ring_budget) return cudaErrorNotSupported;
+  a.stages = ring_budget / a.stage_bytes;
   if (a.stages > kMaxStages) a.stages = kMaxStages;
   a.status = ctx.status;
   a.bias = static_cast<const __half*>(ctx.bias);
@@ -427,15 +501,18 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   a.Af = Af;
   a.Yf = Yf;
   a.biasf = biasf;
+  a.perm = perm;
+  a.Ka = Ka;
   int grid = ctx.num_sms;
   if (grid > N) grid = N;
   const int min_grid = (N + kMaxColsPerCta - 1) / kMaxColsPerCta;
   if (grid < min_grid) grid = min_grid;
-  const size_t smem = (size_t)a.stages * a.stage_bytes;
-  auto kern = select_kernel<PAIR>(wg, cps, bs == 16, s16, zp, af);
+  const size_t smem = (size_t)a.stages * a.stage_bytes + abytes;
+  auto kern = select_kernel<PAIR>(wg, cps, bs == 16, s16, zp, af, ga);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ctx.variant = PAIR ? "gemv_pair_swiglu_tma_ring" : (af ? "gemv_f32_tma_ring" : "gemv_tma_ring");
+  ctx.variant = PAIR ? "gemv_pair_swiglu_tma_ring"
+                     : (af ? "gemv_f32_tma_ring" : (ga ? "gemv_tma_ring_gather" : "gemv_tma_ring"));
   return launch_kernel(ctx, kern, dim3(grid), dim3((kNCW + 1) * 32), smem, a);
 }
 
@@ -455,6 +532,11 @@ cudaError_t launch_gemv_pair_swiglu_tma(LaunchCtx& ctx, const void* A, const QWe
 cudaError_t launch_gemv_f32_tma(LaunchCtx& ctx, const float* A, const QWeight& w, int K, int N, int bs,
                                 float* Y, const float* bias) {
   return launch_tma_impl<false>(ctx, nullptr, &w, K, N, bs, nullptr, A, Y, bias);
+}
+
+cudaError_t launch_gemv_tma_gather(LaunchCtx& ctx, const void* A, const int32_t* perm, int Ka, const QWeight& w,
+                                   int Kp, int N, int bs, void* Y) {
+  return launch_tma_impl<false>(ctx, A, &w, Kp, N, bs, Y, nullptr, nullptr, nullptr, perm, Ka);
 }
 
 }  // namespace mnb

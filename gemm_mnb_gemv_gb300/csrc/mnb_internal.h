@@ -36,6 +36,10 @@ cudaError_t launch_act_order_prepare(LaunchCtx& ctx, const QWeight& w, int K, in
                                      uint8_t* zp_out);
 cudaError_t launch_act_order_gather(LaunchCtx& ctx, const void* A, int M, int K, const int32_t* perm, int Kp,
                                     void* out);
+// M = 1 act-order GEMV with the gather fused into the activation load (one chunk per lane:
+// K' <= 8192); cudaErrorNotSupported otherwise.
+cudaError_t launch_gemv_tma_gather(LaunchCtx& ctx, const void* A, const int32_t* perm, int Ka, const QWeight& w,
+                                   int Kp, int N, int bs, void* Y);
 // Bulk-copy ring GEMV (M = 1); cudaErrorNotSupported when rows are not 16-byte multiples.
 cudaError_t launch_gemv_tma(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs,
                             void* Y);
