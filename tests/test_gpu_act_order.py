@@ -120,6 +120,7 @@ ACT_ORDER_CASES = [
     ("ao_gemv_bal", 1, 4096, 512, 128, "f16", True, "act_order"),
     ("ao_gemv_uneven", 1, 1024, 320, 32, "f32", False, "uneven"),
     ("ao_gemv_uneven16", 1, 512, 129, 16, "f16", True, "uneven"),
+    ("ao_gemv_bigk", 1, 16384, 256, 128, "f16", True, "act_order"),  # K' > 8192: gather pass
     ("ao_small_bal", 4, 2048, 384, 64, "f16", True, "act_order"),
     ("ao_small_uneven", 13, 1024, 200, 32, "f32", True, "uneven"),
     ("ao_tc_bal", 300, 1024, 384, 128, "f16", True, "act_order"),
@@ -142,6 +143,10 @@ def test_gemm_act_order_parity(env, name, M, K, N, bs, sdt, zp, kind):
     assert_within_bound(y.float().cpu().numpy(), Y, B, name)
     variant = mnb.mnb_last_variant()
     assert variant != "act_order_gather", variant  # the product kernel's name is reported
+    if name == "ao_gemv_bal":
+        assert variant == "gemv_tma_ring_gather", variant  # gather fused into the GEMV
+    if name == "ao_gemv_bigk":
+        assert variant == "gemv_tma_ring", variant  # separate gather, then the GEMV
     if M > 16:
         assert variant == tc_variant(N), variant
     mnb.mnb_check_device_status()
