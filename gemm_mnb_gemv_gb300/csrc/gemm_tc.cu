@@ -10,11 +10,12 @@
 // Roles in a 512-thread CTA (one persistent CTA per SM, tiles of 128 n x 256 m):
 //   warp 0      producer: per 64-k stage, a 2-D TMA load of the 256 x 64 activation box
 //               (128-byte swizzle) and a 1-D bulk copy of the 4 KB repacked weight block
-//               into a 5-deep ring (36 KB a slot);
+//               into a 4-deep ring (36 KB a slot);
 //   warp 1      MMA issuer (one lane) and TMEM owner (512 columns: two 256-column
 //               partial accumulators, one per quant group in flight);
 //   warps 4-7   dequantisers: repacked nibbles -> exact fp16 (code - zp) written into one of
-//               two 16 KB weight buffers in the K-major 128-byte-swizzled operand layout;
+//               four 16 KB weight buffers in the K-major 128-byte-swizzled operand layout
+//               (four, so the dequantisers run up to three stages ahead of the MMAs);
 //   warps 8-15  epilogue: per group, read the partial from TMEM, multiply by the group
 //               scale, add into fp32 registers; at the end of a tile, store fp16 Y.
 // Register split (setmaxnreg, warpgroup granularity, launch = 512 x 128):
@@ -36,8 +37,8 @@ namespace {
 constexpr int kTileN = 128;  // weight rows per tile (M_mma)
 constexpr int kTileM = 256;  // activation rows per tile (N_mma)
 constexpr int kStageK = 64;
-constexpr int kStages = 5;                       // activation + packed-weight ring
-constexpr int kWBufs = 2;                        // dequantised-weight buffers
+constexpr int kStages = 4;                       // activation + packed-weight ring
+constexpr int kWBufs = 4;                        // dequantised-weight buffers (<= kStages)
 constexpr int kXBytes = kTileM * kStageK * 2;   // 32 KB
 constexpr int kPBytes = kTileN * kStageK / 2;   // 4 KB
 constexpr int kWBytes = kTileN * kStageK * 2;   // 16 KB
@@ -233,8 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             slot = 0;
             phase ^= 1u;
           }
-          wb ^= 1u;
-          if (wb == 0u) wphase ^= 1u;
+          if (++wb == (uint32_t)kWBufs) {
+            wb = 0u;
+            wphase ^= 1u;
+          }
         }
       }
       tc::mma_commit(&mma_done_bar);
@@ -248,8 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int gshift = 0;           // log2(block size)
     while ((1 << gshift) < p.bs) ++gshift;
     int slot = 0, wb = 0, si = 0;
-    uint32_t phase = 0, wphase = 0;
-    int pslot = 0;          // ring slot of stage si - 2
+    uint32_t phase = 0;
+    int pslot = 0;          // ring slot of stage si - kWBufs
     uint32_t pphase = 0;    // parity of that slot's completed "empty" phase
     bool ok = true;
     const uint32_t w_u32 = smem_u32(smem) + kWOffset;
@@ -257,24 +260,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = t / p.mtiles;
       const int n = nt * kTileN + r;
       // Zero-point byte(s) covering one 64-k stage: one byte for bs >= 32 (two groups at
-      // most, sharing a byte), two bytes for bs = 16.  Fetched one stage ahead.
+      // most, sharing a byte), two bytes for bs = 16.
       auto zp_for = [&](int kb) -> uint32_t {
         const int g0 = (kb * kStageK) >> gshift;
         if (gshift == 4) return zp_byte(p, n, g0 >> 1) | (zp_byte(p, n, (g0 >> 1) + 1) << 8);
         return zp_byte(p, n, g0 >> 1);
       };
-      uint32_t zcur = zp_for(0);
-      for (int kb = 0; kb < p.kblocks; ++kb, ++si) {
-        const uint32_t znext = (kb + 1 < p.kblocks) ? zp_for(kb + 1) : 0u;
-        // The weight buffer was last read by stage si - 2, whose completion is that
+      // One stage: wait for its codes and a free weight buffer, convert, store, announce.
+      auto do_stage = [&](int kb, uint32_t zcur) -> bool {
+        // The weight buffer was last read by stage si - kWBufs, whose completion is that
         // stage's ring-slot "empty" phase.
         if (!mbar_wait_bounded(&full_bar[slot], phase) ||
-            (si >= kWBufs && !mbar_wait_bounded(&empty_bar[pslot], pphase))) {
-          report_status(p.status, kStatusFullWait);
-          atomicExch(&abort_flag, 1);
-          ok = false;
-          break;
-        }
+            (si >= kWBufs && !mbar_wait_bounded(&empty_bar[pslot], pphase)))
+          return false;
         const uint8_t* sp = stage_p(slot);
         const uint32_t sw = w_u32 + (uint32_t)(wb * kWBytes) + (uint32_t)(r * 128);
         const int g0 = (kb * kStageK) >> gshift;
@@ -307,19 +305,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&wready_bar[wb]);
-        zcur = znext;
         if (++slot == kStages) {
           slot = 0;
           phase ^= 1u;
         }
-        wb ^= 1;
-        if (wb == 0) wphase ^= 1u;
-        if (si + 1 >= kWBufs + 1) {  // advance the (si - 2) cursor once si - 2 >= 0 was used
+        if (++wb == kWBufs) wb = 0;
+        if (si >= kWBufs) {  // advance the (si - kWBufs) cursor once it has been used
           if (++pslot == kStages) {
             pslot = 0;
             pphase ^= 1u;
           }
         }
+        ++si;
+        return true;
+      };
+      // Two zero-point registers, one per stage parity, each reloaded two stages ahead right
+      // after its last use, so no register copy ever waits for a global load in flight.
+      uint32_t zeven = zp_for(0);
+      uint32_t zodd = p.kblocks > 1 ? zp_for(1) : 0u;
+      for (int kb = 0; kb < p.kblocks && ok; kb += 2) {
+        if (!do_stage(kb, zeven)) {
+          ok = false;
+          break;
+        }
+        if (kb + 2 < p.kblocks) zeven = zp_for(kb + 2);
+        if (kb + 1 < p.kblocks) {
+          if (!do_stage(kb + 1, zodd)) {
+            ok = false;
+            break;
+          }
+          if (kb + 3 < p.kblocks) zodd = zp_for(kb + 3);
+        }
+      }
+      if (!ok) {
+        report_status(p.status, kStatusFullWait);
+        atomicExch(&abort_flag, 1);
       }
     }
   } else {
