@@ -204,11 +204,10 @@ mnb_status mnb_gemv(const void* A, mnb_weight w, int K, int N, int block_size, v
 }
 
 size_t mnb_workspace_bytes(int M, int K, int N, int block_size) {
-  (void)M;
-  (void)K;
-  (void)N;
-  (void)block_size;
-  return 0;
+  // Only the small-M kernel with K split into slices (K beyond one shared-memory pass)
+  // needs scratch: its fp32 partials.
+  if (M < 2 || M > 16 || K < 1 || N < 1 || K > kMaxKN || N > kMaxKN) return 0;
+  return mnb::smallm_workspace_bytes(M, K, N, block_size);
 }
 
 }  // extern "C"
@@ -218,7 +217,8 @@ namespace {
 // M = 1: GEMV; M > 16: tcgen05 GEMM on the repacked operand; otherwise the small-M
 // kernel.  Shapes no specialised kernel takes go to the generic kernel.
 cudaError_t dispatch_gemm(mnb::LaunchCtx& ctx, const void* A, int M, const mnb::QWeight& q,
-                          const uint8_t* repacked, int K, int N, int bs, void* Y) {
+                          const uint8_t* repacked, int K, int N, int bs, void* Y, void* workspace = nullptr,
+                          size_t ws_bytes = 0) {
   cudaError_t e;
   if (M == 1) {
     e = run_gemv(ctx, A, q, K, N, bs, Y);
@@ -226,7 +226,7 @@ cudaError_t dispatch_gemm(mnb::LaunchCtx& ctx, const void* A, int M, const mnb::
     e = mnb::launch_gemm_tc(ctx, A, M, q, repacked, K, N, bs, Y);
     if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, bs, Y);
   } else {
-    e = mnb::launch_gemm_smallm(ctx, A, M, q, K, N, bs, Y);
+    e = mnb::launch_gemm_smallm(ctx, A, M, q, K, N, bs, Y, workspace, ws_bytes);
     if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, bs, Y);
   }
   return e;
@@ -261,7 +261,7 @@ mnb_status gemm_impl(const char* fn, const void* A, int M, mnb_weight w, const u
   if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
   ctx.bias = bias_mode ? bias : nullptr;
   ctx.bias_mode = bias_mode;
-  return finish(fn, dispatch_gemm(ctx, A, M, q, repacked, K, N, block_size, Y), ctx);
+  return finish(fn, dispatch_gemm(ctx, A, M, q, repacked, K, N, block_size, Y, workspace, ws_bytes), ctx);
 }
 
 }  // namespace

@@ -40,11 +40,18 @@ struct SmArgs {
   const uint8_t* zp;
   __half* Y;
   int M, K, N, G, gshift;
-  int row_bytes;     // K / 2
-  int srow;          // scale bytes per row
-  int zrow;          // zero-point bytes per row (0 if none)
-  int prow;          // staged row stride = row_bytes + kRowPad
-  int stage_bytes;   // kRows * prow + kRows * srow + kRows * zrow (16-aligned)
+  int row_bytes;     // K / 2 (packed row stride in global memory)
+  int srow;          // scale bytes per row in global memory
+  int ssz;           // bytes per scale
+  int zrow;          // zero-point bytes per row (0 if none); staged whole
+  // Split-K: grid.y = nslices slices of kslice k (the last one shorter); a slice stages its
+  // packed codes and scales, and with more than one slice writes fp32 partials to
+  // part[slice][m][n], which combine_slices_kernel adds in slice order.
+  int kslice, nslices;
+  float* part;
+  int sslice;        // staged scale bytes per row (kslice / bs * ssz)
+  int prow;          // staged row stride = kslice / 2 + kRowPad
+  int stage_bytes;   // kRows * (prow + sslice + zrow) (16-aligned)
   int stages;
   int ntiles, tiles_per_cta;
   uint32_t* status;
@@ -85,7 +92,7 @@ __device__ __forceinline__ float slice_sum(const float (&red)[kGW][MSETS][32][4]
   return v;
 }
 
-template <int MSETS, bool S16, bool ZP, bool F32 = false>
+template <int MSETS, bool S16, bool ZP, bool F32 = false, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
@@ -93,7 +100,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
   __shared__ int failed;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int C = p.K >> 5;                 // 32-k chunks
+  const int slice = SPLIT ? (int)blockIdx.y : 0;
+  const int k0 = SPLIT ? slice * p.kslice : 0;     // first k of this slice
+  const int klen = SPLIT ? min(p.kslice, p.K - k0) : p.K;
+  const int C = klen >> 5;                         // 32-k chunks in the slice
+  const int gb = SPLIT ? (k0 >> p.gshift) : 0;     // first group of the slice
   const int S = p.stages;
   // shared memory: [ring stages][activations in fragment order]
   uint8_t* ring = smem_raw;
@@ -126,13 +137,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
         const int n0 = (t_begin + i) * kRows;
         const int nr = min(kRows, p.N - n0);
         uint8_t* st = ring + (size_t)slot * p.stage_bytes;
-        const uint32_t bytes = (uint32_t)nr * (p.row_bytes + p.srow + p.zrow);
+        const int pbytes = klen >> 1, sbytes = (klen >> p.gshift) * p.ssz;
+        const uint32_t bytes = (uint32_t)nr * (pbytes + sbytes + p.zrow);
         mbar_arrive_expect_tx(&full_bar[slot], bytes);
         for (int r = 0; r < nr; ++r)
-          bulk_g2s(st + r * p.prow, p.packed + (long long)(n0 + r) * p.row_bytes, p.row_bytes, &full_bar[slot]);
-        bulk_g2s(st + kRows * p.prow, p.scales + (long long)n0 * p.srow, nr * p.srow, &full_bar[slot]);
+          bulk_g2s(st + r * p.prow, p.packed + (long long)(n0 + r) * p.row_bytes + (k0 >> 1), pbytes,
+                   &full_bar[slot]);
+        if (!SPLIT) {  // whole scale rows: one copy for the tile (sslice == srow)
+          bulk_g2s(st + kRows * p.prow, p.scales + (long long)n0 * p.srow, nr * p.srow, &full_bar[slot]);
+        } else {
+          for (int r = 0; r < nr; ++r)
+            bulk_g2s(st + kRows * p.prow + r * p.sslice, p.scales + (long long)(n0 + r) * p.srow + gb * p.ssz,
+                     sbytes, &full_bar[slot]);
+        }
         if (ZP)
-          bulk_g2s(st + kRows * (p.prow + p.srow), p.zp + (long long)n0 * p.zrow, nr * p.zrow, &full_bar[slot]);
+          bulk_g2s(st + kRows * (p.prow + p.sslice), p.zp + (long long)n0 * p.zrow, nr * p.zrow, &full_bar[slot]);
         ++issued;
         if (++slot == S) {
           slot = 0;
@@ -159,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
       for (int u = 0; u < kBatch; ++u) {
         const int e = e0 + u * kCW * 32;
         const int l = e & 31, c = (e >> 5) % C, s = (e >> 5) / C;
-        const int m = 8 * s + (l >> 2), k = 32 * c + 8 * (l & 3);
+        const int m = 8 * s + (l >> 2), k = k0 + 32 * c + 8 * (l & 3);
         x[u] = make_uint4(0, 0, 0, 0);
         if (e < entries && m < p.M) x[u] = *reinterpret_cast<const uint4*>(p.A + (long long)m * p.K + k);
       }
@@ -193,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
       const uint32_t rowg = st + (uint32_t)(g * p.prow) + 4u * t;
       const uint32_t rowg8 = st + (uint32_t)((g + 8) * p.prow) + 4u * t;
       const uint32_t sbase = st + (uint32_t)(kRows * p.prow);
-      const uint32_t zbase = sbase + (uint32_t)(kRows * p.srow);
+      const uint32_t zbase = sbase + (uint32_t)(kRows * p.sslice);
       // Two independent MMA chains per set (first and second half of each chunk's k).
       float acc[MSETS][4], tmp[MSETS][4], tmp2[MSETS][4];
 #pragma unroll
@@ -216,16 +235,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
       };
       if (ok) {
         for (int c = c_lo; c < c_hi; ++c) {
-          const int grp = (c * 32) >> p.gshift;
+          const int grp = (k0 + c * 32) >> p.gshift;  // absolute group (zero points)
           if (grp != cur) {
             if (cur >= 0) flush();
             cur = grp;
+            const int gl = grp - gb;                     // group within the staged scales
             if (S16) {
-              sg = half_bits_to_float(lds_u16_a(sbase + (uint32_t)(g * p.srow + 2 * grp)));
-              sg8 = half_bits_to_float(lds_u16_a(sbase + (uint32_t)((g + 8) * p.srow + 2 * grp)));
+              sg = half_bits_to_float(lds_u16_a(sbase + (uint32_t)(g * p.sslice + 2 * gl)));
+              sg8 = half_bits_to_float(lds_u16_a(sbase + (uint32_t)((g + 8) * p.sslice + 2 * gl)));
             } else {
-              sg = __uint_as_float(lds_u32_a(sbase + (uint32_t)(g * p.srow + 4 * grp)));
-              sg8 = __uint_as_float(lds_u32_a(sbase + (uint32_t)((g + 8) * p.srow + 4 * grp)));
+              sg = __uint_as_float(lds_u32_a(sbase + (uint32_t)(g * p.sslice + 4 * gl)));
+              sg8 = __uint_as_float(lds_u32_a(sbase + (uint32_t)((g + 8) * p.sslice + 4 * gl)));
             }
             if (ZP) {
               const uint32_t sh = (uint32_t)(grp & 1) * 4u;
@@ -281,7 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
         for (int w = 0; w < kGW; ++w) v += red[gi][w][s][l][j];
         const int n = n0 + row;
         if (m < p.M && n < p.N) {
-          p.Y[(long long)m * p.N + n] = failed ? __ushort_as_half(0x7e00) : round_out(v, p.bias, n, p.bias_mode);
+          if constexpr (SPLIT)
+            p.part[((long long)slice * p.M + m) * p.N + n] = failed ? __uint_as_float(0x7fc00000u) : v;
+          else
+            p.Y[(long long)m * p.N + n] = failed ? __ushort_as_half(0x7e00) : round_out(v, p.bias, n, p.bias_mode);
         }
       }
       group_bar(gi);
@@ -289,16 +312,62 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
   }
 }
 
-using SmKernel = void (*)(const SmArgs);
-
-template <int MSETS, bool F32>
-SmKernel pick(bool s16, bool zp) {
-  if (s16) return zp ? gemm_smallm_kernel<MSETS, true, true, F32> : gemm_smallm_kernel<MSETS, true, false, F32>;
-  return zp ? gemm_smallm_kernel<MSETS, false, true, F32> : gemm_smallm_kernel<MSETS, false, false, F32>;
+// Fixed-order sum of the split-K partials, then the fp16 epilogue (bias modes).
+__global__ void __launch_bounds__(256) combine_slices_kernel(const float* __restrict__ part, int nslices,
+                                                             long long mn, int N, __half* __restrict__ Y,
+                                                             const __half* bias, int bias_mode) {
+  pdl_launch_dependents();
+  pdl_wait();
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < mn; i += (long long)gridDim.x * blockDim.x) {
+    float v = 0.0f;
+    for (int s = 0; s < nslices; ++s) v += part[s * mn + i];
+    Y[i] = round_out(v, bias, (int)(i % N), bias_mode);
+  }
 }
 
+using SmKernel = void (*)(const SmArgs);
+
+template <int MSETS, bool F32, bool SPLIT = false>
+SmKernel pick(bool s16, bool zp) {
+  if (s16)
+    return zp ? gemm_smallm_kernel<MSETS, true, true, F32, SPLIT> : gemm_smallm_kernel<MSETS, true, false, F32, SPLIT>;
+  return zp ? gemm_smallm_kernel<MSETS, false, true, F32, SPLIT> : gemm_smallm_kernel<MSETS, false, false, F32, SPLIT>;
+}
+
+}  // namespace
+
+// K-slice length for the small-M kernel: all of K when its rows, scales and activations fit
+// two ring slots, else the largest of 4096 / 2048 / 1024 (multiples of the block size) that
+// fits.  ssz: bytes per scale; zp: zero points present.  0: not handled.
+int smallm_kslice(int M, int K, int bs, int ssz, bool zp) {
+  if (M < 2 || M > 16 || bs < 32 || K % 32 != 0) return 0;
+  const int msets = M <= 8 ? 1 : 2;
+  const int G = K / bs, zrow = zp ? (G + 1) / 2 : 0;
+  auto fits = [&](int ks) {
+    const size_t stage = (size_t)kRows * (ks / 2 + kRowPad + (ks / bs) * ssz + zrow);
+    const size_t xbytes = (size_t)msets * (ks / 32) * 32 * 16;
+    return xbytes + 2 * stage <= (size_t)kSmemBudget;
+  };
+  if (fits(K)) return K;
+  for (int ks : {4096, 2048, 1024})
+    if (ks < K && ks % bs == 0 && fits(ks)) return ks;
+  return 0;
+}
+
+// Upper bound over the scale dtype and zero points: the slicing with fp32 scales and zero
+// points (the largest footprint, hence the most slices) needs the most partials.
+size_t smallm_workspace_bytes(int M, int K, int N, int bs) {
+  const int ks = smallm_kslice(M, K, bs, 4, true);
+  if (ks == 0 || ks >= K) return 0;
+  const size_t ns = (size_t)((K + ks - 1) / ks);
+  return ns * (size_t)M * (size_t)N * 4;
+}
+
+namespace {
+
 cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
-                               void* Y, int Mout, float* Yf, const float* biasf, const int* rexp) {
+                               void* Y, int Mout, float* Yf, const float* biasf, const int* rexp,
+                               void* workspace = nullptr, size_t ws_bytes = 0) {
   if (M < 2 || M > 16 || bs < 32 || K % 32 != 0) return cudaErrorNotSupported;
   SmArgs a = {};
   a.A = static_cast<const __half*>(A);
@@ -313,18 +382,39 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   a.gshift = 0;
   while ((1 << a.gshift) < bs) ++a.gshift;
   a.row_bytes = K / 2;
-  a.srow = a.G * (w.scales_f16 ? 2 : 4);
+  a.ssz = w.scales_f16 ? 2 : 4;
+  a.srow = a.G * a.ssz;
   a.zrow = w.zp ? (a.G + 1) / 2 : 0;
-  if (a.srow % 16 != 0 || a.zrow % 16 != 0) return cudaErrorNotSupported;
-  a.prow = a.row_bytes + kRowPad;
-  a.stage_bytes = kRows * (a.prow + a.srow + a.zrow);
+  const int ks = smallm_kslice(M, K, bs, a.ssz, w.zp != nullptr);
+  if (ks == 0) return cudaErrorNotSupported;
+  a.kslice = ks;
+  a.nslices = (K + ks - 1) / ks;
+  const int klast = K - (a.nslices - 1) * ks;
+  a.sslice = (ks / bs) * a.ssz;
+  // Every bulk copy is a 16-byte multiple at a 16-byte offset: packed slices (k multiples
+  // of 32), scale slices (checked here, also the last one, and the row stride) and a tile's
+  // zero-point rows (16 * zrow bytes at a multiple of 16 * zrow: any zrow works for whole
+  // tiles; a partial last tile needs zrow itself to be a multiple of 16).
+  if (a.sslice % 16 != 0 || ((klast / bs) * a.ssz) % 16 != 0 || a.srow % 16 != 0 ||
+      (a.zrow % 16 != 0 && N % kRows != 0))
+    return cudaErrorNotSupported;
+  if (a.nslices > 1) {
+    // fp32-output (split activation) calls use one slice; more need the partials workspace.
+    if (Yf != nullptr) return cudaErrorNotSupported;
+    if (workspace == nullptr || ws_bytes < (size_t)a.nslices * M * N * 4) return cudaErrorNotSupported;
+    a.part = static_cast<float*>(workspace);
+  }
+  a.prow = ks / 2 + kRowPad;
+  a.stage_bytes = kRows * (a.prow + a.sslice + a.zrow);
   const int msets = M <= 8 ? 1 : 2;
-  const size_t xbytes = (size_t)msets * (K / 32) * 32 * 16;
+  const size_t xbytes = (size_t)msets * (ks / 32) * 32 * 16;
   if ((size_t)kSmemBudget < xbytes + 2 * (size_t)a.stage_bytes) return cudaErrorNotSupported;
   a.stages = (int)((kSmemBudget - xbytes) / a.stage_bytes);
   if (a.stages > kMaxStages) a.stages = kMaxStages;
   a.ntiles = (N + kRows - 1) / kRows;
-  a.tiles_per_cta = (a.ntiles + ctx.num_sms - 1) / ctx.num_sms;
+  // Spread (tile, slice) units over the SMs: each slice gets num_sms / nslices CTAs.
+  const int ctas_per_slice = ctx.num_sms / a.nslices > 0 ? ctx.num_sms / a.nslices : 1;
+  a.tiles_per_cta = (a.ntiles + ctas_per_slice - 1) / ctas_per_slice;
   const int grid = (a.ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta;
   a.status = ctx.status;
   a.bias = static_cast<const __half*>(ctx.bias);
@@ -336,19 +426,28 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   const bool f32 = Yf != nullptr;
   const size_t smem = (size_t)a.stages * a.stage_bytes + xbytes;
   const bool s16 = w.scales_f16 != 0, zp = w.zp != nullptr;
-  SmKernel kern = msets == 1 ? (f32 ? pick<1, true>(s16, zp) : pick<1, false>(s16, zp))
-                             : (f32 ? pick<2, true>(s16, zp) : pick<2, false>(s16, zp));
+  const bool split = a.nslices > 1;  // fp32-output calls never split
+  SmKernel kern = msets == 1 ? (f32 ? pick<1, true>(s16, zp) : (split ? pick<1, false, true>(s16, zp) : pick<1, false>(s16, zp)))
+                             : (f32 ? pick<2, true>(s16, zp) : (split ? pick<2, false, true>(s16, zp) : pick<2, false>(s16, zp)));
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ctx.variant = f32 ? "gemm_smallm_mma16816_f32split" : "gemm_smallm_mma16816";
-  return launch_kernel(ctx, kern, dim3(grid), dim3(kThreads), smem, a);
+  if (a.nslices == 1) return launch_kernel(ctx, kern, dim3(grid), dim3(kThreads), smem, a);
+  e = launch_kernel(ctx, kern, dim3(grid, a.nslices), dim3(kThreads), smem, a);
+  if (e != cudaSuccess) return e;
+  const long long mn = (long long)M * N;
+  const long long blocks = (mn + 255) / 256, cap = (long long)ctx.num_sms * 8;
+  ctx.variant = "gemm_smallm_mma16816_splitk";
+  return launch_kernel(ctx, combine_slices_kernel, dim3((unsigned)(blocks < cap ? blocks : cap)), dim3(256), 0,
+                       static_cast<const float*>(a.part), a.nslices, mn, N, static_cast<__half*>(Y),
+                       static_cast<const __half*>(ctx.bias), ctx.bias_mode);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
-                               void* Y) {
-  return launch_smallm_impl(ctx, A, M, w, K, N, bs, Y, M, nullptr, nullptr, nullptr);
+                               void* Y, void* workspace, size_t ws_bytes) {
+  return launch_smallm_impl(ctx, A, M, w, K, N, bs, Y, M, nullptr, nullptr, nullptr, workspace, ws_bytes);
 }
 
 cudaError_t launch_gemm_smallm_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w, int K, int N,

@@ -50,9 +50,13 @@ cudaError_t launch_gemv(LaunchCtx& ctx, const void* A, const QWeight& w, int K, 
                         void* Y);
 cudaError_t launch_gemv_pair_swiglu(LaunchCtx& ctx, const void* A, const QWeight& gate,
                                     const QWeight& up, int K, int N, int bs, void* out);
-// 2 <= M <= 16 (block size >= 32): weights streamed once, mma.sync over M rows.
+// 2 <= M <= 16 (block size >= 32): weights streamed once, mma.sync over M rows.  For K
+// beyond one shared-memory pass the K range is split into slices whose fp32 partials go to
+// `workspace` (smallm_workspace_bytes of it) and are summed in slice order.
 cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
-                               void* Y);
+                               void* Y, void* workspace, size_t ws_bytes);
+int smallm_kslice(int M, int K, int bs, int ssz, bool zp);
+size_t smallm_workspace_bytes(int M, int K, int N, int bs);
 // M > 16 on the tcgen05 tensor cores, reading the repacked operand.
 cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& w,
                            const uint8_t* repacked, int K, int N, int bs, void* Y);

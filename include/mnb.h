@@ -118,8 +118,13 @@ MNB_API mnb_status mnb_gemv(const void *A, mnb_weight w, int K, int N, int block
                     mnb_stream stream);
 
 /*
- * Scratch bytes mnb_gemm needs for this shape (0 when none). The caller allocates it
- * once and passes it to every call of that shape; its contents need no initialisation.
+ * Scratch bytes mnb_gemm (and mnb_gemm_bias) needs for this shape (0 when none). Only
+ * 2 <= M <= 16 with K too large for one shared-memory pass of the small-M kernel needs
+ * any: K is then split into slices whose fp32 partials ([slices, M, N]) are summed in
+ * slice order, so results stay deterministic. The size is an upper bound over the scale
+ * dtype and zero points (the call may use less). The caller allocates it once and passes it
+ * to every call of that shape; its contents need no initialisation, each call overwrites
+ * them, so calls sharing one workspace must be ordered on one stream.
  */
 MNB_API size_t mnb_workspace_bytes(int M, int K, int N, int block_size);
 

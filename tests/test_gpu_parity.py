@@ -455,3 +455,52 @@ def test_bias_mode_validation(env):
     with pytest.raises(mnb.MnbError) as e:
         mnb.mnb_gemm_bias(a, packed, scales, None, 64, 8, 32, torch.zeros(8, dtype=torch.float16, device=dev), 5)
     assert e.value.status == mnb.MNB_ERR_INVALID_ARG
+
+
+# Small M with K beyond one shared-memory pass: K split into slices, fp32 partials in the
+# workspace, summed in slice order.
+SPLITK_CASES = [
+    (2, 14336, 4096, 32, "f32", False),   # the down projection at speculative-verify M
+    (5, 8192, 200, 64, "f16", True),
+    (13, 12288, 96, 128, "f32", True),
+    (3, 14336, 144, 128, "f16", True),    # last slice 2048 of 4096; zero-point rows of 56 bytes
+    (16, 10240, 64, 32, "f16", False),
+]
+
+
+@pytest.mark.parametrize("M,K,N,bs,sdt,zp", SPLITK_CASES)
+def test_gemm_small_m_split_k(env, M, K, N, bs, sdt, zp):
+    mnb, torch, dev = env
+    wl = syn.custom(f"sk_{M}_{K}_{N}_{bs}", M, K, N, bs, scales_dtype=sdt, has_zp=zp)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    need = mnb.mnb_workspace_bytes(M, K, N, bs)
+    assert need > 0
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=dev)  # stale contents must not matter
+    y = mnb.mnb_gemm(upload_act(A, dev), *upload_weight(w, dev), K, N, bs, workspace=ws)
+    torch.cuda.synchronize()
+    assert mnb.mnb_last_variant() == "gemm_smallm_mma16816_splitk"
+    mnb.mnb_check_device_status()
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
+    assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
+
+
+def test_gemm_small_m_split_k_bias_and_repeat(env):
+    mnb, torch, dev = env
+    M, K, N, bs = 4, 12288, 256, 64
+    wl = syn.custom("sk_bias", M, K, N, bs)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    bias = (syn.normal(syn.fnv1a64("sk_bias/bias"), N) * 0.5).astype(np.float16)
+    a, wt, b = upload_act(A, dev), upload_weight(w, dev), upload_act(bias, dev)
+    ws = torch.empty(mnb.mnb_workspace_bytes(M, K, N, bs), dtype=torch.uint8, device=dev)
+    y0 = mnb.mnb_gemm(a, *wt, K, N, bs, workspace=ws)
+    y2 = mnb.mnb_gemm_bias(a, *wt, K, N, bs, b, mnb.MNB_BIAS_AFTER_ROUND, workspace=ws)
+    y0b = mnb.mnb_gemm(a, *wt, K, N, bs, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y0b)  # deterministic across calls
+    assert torch.equal(y2, (y0.float() + b.float()).half())
+    # a workspace smaller than stated is refused
+    small = torch.empty(16, dtype=torch.uint8, device=dev)
+    with pytest.raises(mnb.MnbError):
+        mnb.mnb_gemm(a, *wt, K, N, bs, workspace=small)
