@@ -53,6 +53,9 @@ struct TmaGemvArgs {
   // Act-order gather (GA): activation k' is A[perm[k']] (0 where perm = -1), A of Ka halves.
   const int32_t* perm;
   int Ka;
+  // Zero points read from global memory (ZG): rows of zrb_g bytes that are not 16-byte
+  // multiples cannot be bulk-copied per stage; the stage then has no zero-point region.
+  int zrb_g;
 };
 
 __device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
@@ -84,7 +87,7 @@ __device__ __forceinline__ float dot_word_f32(uint32_t w, uint32_t zlo, uint32_t
 }
 
 template <int NCW, int WG, int CPS, int VPG, bool BS16, bool PAIR, bool S16, bool ZP, bool AF = false,
-          bool GA = false>
+          bool GA = false, bool ZG = false>
 __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
     gemv_tma_kernel(const TmaGemvArgs p) {
   constexpr int kThreads = (NCW + 1) * 32;
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
           uint8_t* wb = base + t * wt_stride;
           bulk_g2s(wb, p.packed[t] + (long long)col * p.row_bytes, nc * p.row_bytes, &full_bar[slot]);
           bulk_g2s(wb + reg_p, p.scales[t] + (long long)col * p.sbytes, nc * p.sbytes, &full_bar[slot]);
-          if (ZP)
+          if (ZP && !ZG)
             bulk_g2s(wb + reg_p + reg_s, p.zp[t] + (long long)col * p.zbytes, nc * p.zbytes,
                      &full_bar[slot]);
         }
@@ -260,13 +263,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
     int slot = 0;
     uint32_t phase = 0;
     for (int st = 0; st < nstages_total; ++st) {
+      const int col0 = n0 + st * CB;
+      const int nc = min(CB, n1 - col0);
+      // ZG: this stage's zero-point bytes, loaded before its wait so the latency overlaps it.
+      uint32_t zg[ZG ? VPG : 1][ZG ? CPS : 1];
+      if constexpr (ZG) {
+#pragma unroll
+        for (int vi = 0; vi < VPG; ++vi) {
+          const int ci = g + vi * NG;
+#pragma unroll
+          for (int j = 0; j < CPS; ++j)
+            zg[vi][j] = (ci < nc && cval[j]) ? ld_nc_u8(p.zp[0] + (long long)(col0 + ci) * p.zrb_g + zofs[j]) : 0x88u;
+        }
+      }
       if (ok && !mbar_wait_bounded(&full_bar[slot], phase)) {
         report_status(p.status, kStatusFullWait);
         atomicExch(&failed, 1);
         ok = false;
       }
-      const int col0 = n0 + st * CB;
-      const int nc = min(CB, n1 - col0);
       const uint32_t sb = ring_u32 + (uint32_t)(slot * p.stage_bytes);
       float part[V];
 #pragma unroll
@@ -283,7 +297,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
           for (int j = 0; j < CPS; ++j) {
             if (live && cval[j]) {
               const uint4 w4 = lds128_a(cp + wofs[j]);
-              const uint32_t zb = ZP ? lds_u8_a(cz + zofs[j]) : 0x88u;
+              uint32_t zb = 0x88u;
+              if constexpr (ZG) zb = zg[vi][j];
+              else if constexpr (ZP) zb = lds_u8_a(cz + zofs[j]);
               if (BS16) {
                 const uint32_t z0 = zb & 15u, z1 = zb >> 4;
                 const uint32_t zl0 = ZP ? zp_lo_const(z0) : zl8, zh0 = ZP ? zp_hi_const(z0) : zh8;
@@ -414,6 +430,15 @@ TmaKernel pick_af(bool bs16, bool s16, bool zp) {
 #undef MNB_PICK
 }
 
+// Zero points from global memory (single weight, fp16 activations).
+template <int WG, int CPS>
+TmaKernel pick_zg(bool bs16, bool s16) {
+#define MNB_PICK(B, S) gemv_tma_kernel<kNCW, WG, CPS, 4, B, false, S, true, false, false, true>
+  if (bs16) return s16 ? MNB_PICK(true, true) : MNB_PICK(true, false);
+  return s16 ? MNB_PICK(false, true) : MNB_PICK(false, false);
+#undef MNB_PICK
+}
+
 // Act-order gather (single weight, one chunk per lane).
 template <int WG>
 TmaKernel pick_ga(bool bs16, bool s16, bool zp) {
@@ -428,7 +453,11 @@ TmaKernel pick_ga(bool bs16, bool s16, bool zp) {
 }
 
 template <bool PAIR>
-TmaKernel select_kernel(int wg, int cps, bool bs16, bool s16, bool zp, bool af, bool ga) {
+TmaKernel select_kernel(int wg, int cps, bool bs16, bool s16, bool zp, bool af, bool ga, bool zgl) {
+  if (zgl) {
+    if (wg == 4) return pick_zg<4, 1>(bs16, s16);
+    return cps == 1 ? pick_zg<8, 1>(bs16, s16) : pick_zg<8, 2>(bs16, s16);
+  }
   if (ga) return wg == 4 ? pick_ga<4>(bs16, s16, zp) : pick_ga<8>(bs16, s16, zp);
   if (af) {
     if (wg == 4) return pick_af<4, 1>(bs16, s16, zp);
@@ -481,6 +510,14 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   while (bs >= 32 && (32 << a.group_shift) < bs) ++a.group_shift;
   a.sbytes = G * (s16 ? 2 : 4);
   a.zbytes = zp ? (G + 1) / 2 : 0;
+  a.zrb_g = a.zbytes;
+  // Zero-point rows that are not 16-byte multiples: read from global memory instead of
+  // staged (single fp16-activation weight only).
+  const bool zgl = zp && a.zbytes % 16 != 0 && !PAIR && !af && !ga;
+  if (zgl) {
+    if (cps > 2) return cudaErrorNotSupported;  // keeps the per-stage zero points in registers
+    a.zbytes = 0;
+  }
   if (a.sbytes % 16 != 0 || a.zbytes % 16 != 0) return cudaErrorNotSupported;
   for (int t = 0; t < 2; ++t) {
     const QWeight& q = w[t < NWT ? t : 0];
@@ -508,7 +545,7 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   const int min_grid = (N + kMaxColsPerCta - 1) / kMaxColsPerCta;
   if (grid < min_grid) grid = min_grid;
   const size_t smem = (size_t)a.stages * a.stage_bytes + abytes;
-  auto kern = select_kernel<PAIR>(wg, cps, bs == 16, s16, zp, af, ga);
+  auto kern = select_kernel<PAIR>(wg, cps, bs == 16, s16, zp, af, ga, zgl);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ctx.variant = PAIR ? "gemv_pair_swiglu_tma_ring"

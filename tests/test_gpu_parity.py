@@ -82,6 +82,10 @@ GEMV_CASES = [
     ("gv_k32768", 32768, 70, 128, "f16", False, "normal"),
     ("gv_generic_k48", 48, 5, 16, "f16", True, "normal"),
     ("gv_generic_k65536", 65536, 9, 64, "f16", True, "normal"),
+    # zero-point rows that are not 16-byte multiples (4, 28, 56 bytes): read from global
+    ("gv_zrow4", 1024, 150, 128, "f16", True, "normal"),
+    ("gv_zrow28", 3584, 200, 64, "f32", True, "normal"),
+    ("gv_zrow56_down", 14336, 1000, 128, "f16", True, "normal"),
 ]
 
 
@@ -98,6 +102,10 @@ def test_gemv_parity(env, name, K, N, bs, sdt, zp, act):
     assert_within_bound(y.cpu().numpy()[None, :], Y, B, name)
     expect_generic = (K % 32 != 0) or K > 32768
     assert variant.startswith("generic") == expect_generic, variant
+    if name in ("gv_one_col", "gv_ragged32"):  # scale rows of 8 and 6 bytes
+        assert variant == "gemv_f16acc32", variant
+    if name.startswith("gv_zrow"):
+        assert variant == "gemv_tma_ring", variant
 
 
 @pytest.mark.parametrize("wname", ["tiny_gemv_k256_n128", "gemv_attnproj_k4096_n4096",
@@ -339,9 +347,12 @@ def test_programmatic_launch_gives_same_bits(env):
         assert torch.equal(b, p)
 
 
+# tiny_gemv: 4-byte zero-point rows, read from global by the streaming kernel; the
+# register-pipelined kernel still takes scale rows that are not 16-byte multiples
+# (gv_one_col, gv_ragged32 in GEMV_CASES).
 @pytest.mark.parametrize("wname,variant", [("gemv_attnproj_k4096_n4096", "gemv_tma_ring"),
                                            ("mlp_down_k14336_n4096", "gemv_tma_ring"),
-                                           ("tiny_gemv_k256_n128", "gemv_f16acc32")])
+                                           ("tiny_gemv_k256_n128", "gemv_tma_ring")])
 def test_gemv_dispatch_picks_the_streaming_kernel(env, wname, variant):
     mnb, torch, dev = env
     wl = syn.WORKLOADS[wname]
