@@ -303,13 +303,16 @@ class DeviceBench:
                 "gbps": call_bytes(wl) / (us * 1e3), "copies": ncopy,
                 "variant": variant if variant.endswith("_gather") else "act_order_gather + " + variant}
 
-    def gemm(self, wl, steps, warmup, sampler, calls, repacked: bool):
+    def gemm(self, wl, steps, warmup, sampler, calls, repacked: bool, shared_act: bool = False):
+        """shared_act: one activation block for every call (a decode-time verify step reads the
+        rows the previous op just wrote, so they sit in L2); otherwise each weight copy has its
+        own activation copy and both come from HBM."""
         torch, mnb = self.torch, self.mnb
-        per_copy = weight_bytes(wl) + wl.M * wl.K * 2
+        per_copy = weight_bytes(wl) + (0 if shared_act else wl.M * wl.K * 2)
         ncopy = self.copies_for(per_copy)
         _, copies = self.upload_weights(wl, "B", ncopy)
         A0 = torch.from_numpy(syn.make_activation(wl)).to(self.dev)
-        As = [A0] + [A0.clone() for _ in range(ncopy - 1)]
+        As = [A0] * ncopy if shared_act else [A0] + [A0.clone() for _ in range(ncopy - 1)]
         rps = [mnb.mnb_repack(c[0], wl.K, wl.N, wl.block_size) if repacked else None for c in copies]
         Y = torch.empty((wl.M, wl.N), dtype=torch.float16, device=self.dev)
         need = mnb.mnb_workspace_bytes(wl.M, wl.K, wl.N, wl.block_size)
@@ -325,7 +328,8 @@ class DeviceBench:
         us = ms * 1e3 / calls
         return {"workload": wl.name, "M": wl.M, "us_per_call": us,
                 "gbps": call_bytes(wl) / (us * 1e3), "tflops": call_flops(wl) / (us * 1e6),
-                "copies": ncopy, "variant": mnb.mnb_last_variant()}
+                "copies": ncopy, "activations": "shared (L2-resident)" if shared_act else "rotated with the weights",
+                "variant": mnb.mnb_last_variant()}
 
     def gemm_f32(self, wl, steps, warmup, sampler, calls):
         """fp32 activations and output: the fp32 GEMV at M = 1, the split-activation
@@ -485,7 +489,10 @@ def run_single(db, name, steps, warmup):
     if name == "down":
         return db.gemv(W["mlp_down_k14336_n4096"], steps, warmup, None, calls=200)
     if name.startswith("verify_m"):
-        return db.gemm(W[f"{name}_k4096_n4096"], steps, warmup, None, calls=200, repacked=False)
+        rot = name.endswith("_rot")  # activations rotated with the weight copies
+        base = name[:-4] if rot else name
+        return db.gemm(W[f"{base}_k4096_n4096"], steps, warmup, None, calls=200, repacked=False,
+                       shared_act=not rot)
     if name == "mlp_chain":
         return db.mlp_chain(steps, warmup, None)
     if name == "act_order_attn":
@@ -509,7 +516,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, short CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
-                    help="time one workload only (attn, gate_up, down, verify_m2/4/8/16, prefill, mlp_chain, "
+                    help="time one workload only (attn, gate_up, down, verify_m2/4/8/16 [_rot: activations rotated "
+                         "with the weights], prefill, mlp_chain, "
                          "act_order_attn, f32_attn, f32_prefill) "
                          "and print its record; for profiling")
     args = ap.parse_args()
@@ -561,7 +569,7 @@ def main():
         del d
         for M in (2, 4, 8, 16):
             extras[f"verify_m{M}"] = db.gemm(syn.WORKLOADS[f"verify_m{M}_k4096_n4096"], 20, 3, sampler,
-                                             calls=200, repacked=False)
+                                             calls=200, repacked=False, shared_act=True)
         extras["prefill"] = db.gemm(syn.WORKLOADS["prefill_m2048_k4096_n14336"], 10, 3, sampler,
                                     calls=9, repacked=True)
         extras["mlp_chain"] = db.mlp_chain(10, 3, sampler)

@@ -15,9 +15,13 @@
 // (g, t) supplies physical k = 8t + {0,4,1,5} to the first MMA and 8t + {2,6,3,7} to the
 // second, which is exactly the pairing the magic-number conversion produces, so no
 // register shuffles are needed.  Each MMA spans one 32-k chunk, inside one quant group
-// for block sizes >= 32; per group the fresh fp32 fragment is multiplied by the group
-// scale of its row and added to the running sum (scale after accumulate, as in
-// matmul_nbits_marlin_gemm_f16 of marlin_gemm.rs).
+// for block sizes >= 32.  A warp walks its K range group by group (1, 2 or 4 chunks per
+// group, a template parameter): it reads the group's scale and zero point of its two rows
+// once, accumulates the group's MMAs into a fresh fp32 fragment and adds that fragment
+// times the group scale to the running sum (scale after accumulate, as in
+// matmul_nbits_marlin_gemm_f16 of marlin_gemm.rs).  Staged scale rows are padded to a
+// stride of 16 mod 32 bytes so the eight rows a warp reads together sit in eight banks,
+// and lanes whose activation row is past M skip their activation reads.
 #include "mnb_device.cuh"
 #include "mnb_internal.h"
 
@@ -49,9 +53,11 @@ struct SmArgs {
   // part[slice][m][n], which combine_slices_kernel adds in slice order.
   int kslice, nslices;
   float* part;
-  int sslice;        // staged scale bytes per row (kslice / bs * ssz)
+  int sslice;        // scale bytes per row of a slice (kslice / bs * ssz)
+  int sstride;       // staged scale row stride: sslice rounded up to 16 mod 32 bytes, so the
+                     // eight rows a warp reads for one group fall in eight different banks
   int prow;          // staged row stride = kslice / 2 + kRowPad
-  int stage_bytes;   // kRows * (prow + sslice + zrow) (16-aligned)
+  int stage_bytes;   // kRows * (prow + sstride + zrow) (16-aligned)
   int stages;
   int ntiles, tiles_per_cta;
   uint32_t* status;
@@ -92,7 +98,19 @@ __device__ __forceinline__ float slice_sum(const float (&red)[kGW][MSETS][32][4]
   return v;
 }
 
-template <int MSETS, bool S16, bool ZP, bool F32 = false, bool SPLIT = false>
+// One m16n8k16 step: c (+)= A . B with the fragment registers of one 32-bit word pair.
+__device__ __forceinline__ void mma16816_zero(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  const float z = 0.0f;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
+// CPG: 32-k chunks per quant group (block size 32, 64 or 128).  The scale dtype is a
+// runtime property (one uniform branch per group); zero points are a template flag.
+template <int MSETS, int CPG, bool ZP, bool F32 = false, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
@@ -143,15 +161,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
         for (int r = 0; r < nr; ++r)
           bulk_g2s(st + r * p.prow, p.packed + (long long)(n0 + r) * p.row_bytes + (k0 >> 1), pbytes,
                    &full_bar[slot]);
-        if (!SPLIT) {  // whole scale rows: one copy for the tile (sslice == srow)
-          bulk_g2s(st + kRows * p.prow, p.scales + (long long)n0 * p.srow, nr * p.srow, &full_bar[slot]);
-        } else {
-          for (int r = 0; r < nr; ++r)
-            bulk_g2s(st + kRows * p.prow + r * p.sslice, p.scales + (long long)(n0 + r) * p.srow + gb * p.ssz,
-                     sbytes, &full_bar[slot]);
-        }
+        for (int r = 0; r < nr; ++r)
+          bulk_g2s(st + kRows * p.prow + r * p.sstride, p.scales + (long long)(n0 + r) * p.srow + gb * p.ssz,
+                   sbytes, &full_bar[slot]);
         if (ZP)
-          bulk_g2s(st + kRows * (p.prow + p.sslice), p.zp + (long long)n0 * p.zrow, nr * p.zrow, &full_bar[slot]);
+          bulk_g2s(st + kRows * (p.prow + p.sstride), p.zp + (long long)n0 * p.zrow, nr * p.zrow, &full_bar[slot]);
         ++issued;
         if (++slot == S) {
           slot = 0;
@@ -166,39 +180,61 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
     // ------------------------------ consumers -----------------------------------
     pdl_launch_dependents();
     pdl_wait();
+    const uint32_t xs_u32 = smem_u32(xs);
     // Stage the activations once: entry (set s, chunk c, lane l = 4g + t) holds
-    // A[8s + g][32c + 8t .. +8], paired (x0,x4)(x1,x5)(x2,x6)(x3,x7).
-    // Eight loads in flight per thread before any is used, so the L2 latency is paid once
-    // per batch rather than once per entry.
-    const int entries = MSETS * C * 32;
-    constexpr int kBatch = 8;
-    for (int e0 = tid; e0 < entries; e0 += kBatch * kCW * 32) {
-      uint4 x[kBatch];
+    // A[8s + g][k0 + 32c + 8t .. +8], paired (x0,x4)(x1,x5)(x2,x6)(x3,x7); rows m >= M are
+    // zero.  Warp w fills chunks w, w + kCW, ..., with up to kBatch loads per set in flight
+    // before the first store.
+    {
+      constexpr int kBatch = 8;
+      bool live[MSETS];
+      const __half* arow[MSETS];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = e0 + u * kCW * 32;
-        const int l = e & 31, c = (e >> 5) % C, s = (e >> 5) / C;
-        const int m = 8 * s + (l >> 2), k = k0 + 32 * c + 8 * (l & 3);
-        x[u] = make_uint4(0, 0, 0, 0);
-        if (e < entries && m < p.M) x[u] = *reinterpret_cast<const uint4*>(p.A + (long long)m * p.K + k);
+      for (int s = 0; s < MSETS; ++s) {
+        const int m = 8 * s + (lane >> 2);
+        live[s] = m < p.M;
+        arow[s] = p.A + (long long)(live[s] ? m : 0) * p.K + k0 + 8 * (lane & 3);
       }
+      for (int cb = warp; cb < C; cb += kBatch * kCW) {
+        uint4 x[MSETS][kBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = e0 + u * kCW * 32;
-        if (e < entries) {
-          uint32_t q[4];
-          pair_halves_stride4(x[u], q);
-          *reinterpret_cast<uint4*>(xs + (size_t)e * 16) = make_uint4(q[0], q[1], q[2], q[3]);
-        }
+        for (int s = 0; s < MSETS; ++s)
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const int c = cb + u * kCW;
+            x[s][u] = make_uint4(0, 0, 0, 0);
+            if (live[s] && c < C) x[s][u] = *reinterpret_cast<const uint4*>(arow[s] + 32 * c);
+          }
+#pragma unroll
+        for (int s = 0; s < MSETS; ++s)
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const int c = cb + u * kCW;
+            if (c < C) {
+              uint32_t q[4];
+              pair_halves_stride4(x[s][u], q);
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                               xs_u32 + (uint32_t)(((s * C + c) * 32 + lane) * 16)),
+                           "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
+                           : "memory");
+            }
+          }
       }
     }
     consumer_bar();
 
     const int g = lane >> 2, t = lane & 3;
     const int gi = warp / kGW, gw = warp % kGW;  // tile group, warp within it
-    const int c_lo = (gw * C) / kGW, c_hi = ((gw + 1) * C) / kGW;
-    const uint32_t xs_u32 = smem_u32(xs);
+    const int Gs = C / CPG;                      // quant groups in the slice
+    const int q_lo = (gw * Gs) / kGW, q_hi = ((gw + 1) * Gs) / kGW;  // this warp's groups
+    const bool s16 = p.ssz == 2;
     const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
+    // Per chunk, this lane's activation fragments sit 512 bytes apart; per set, C * 512.
+    // Lanes whose activation row is past M hold zeros and skip the shared-memory read.
+    const uint32_t xlane = xs_u32 + (uint32_t)lane * 16u;
+    bool xlive[MSETS];
+#pragma unroll
+    for (int s = 0; s < MSETS; ++s) xlive[s] = 8 * s + g < p.M;
     bool ok = true;
     for (int i = gi; i < ntile; i += kGroups) {
       const int slot = i % S;
@@ -211,65 +247,76 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
       const uint32_t st = smem_u32(ring + (size_t)slot * p.stage_bytes);
       const uint32_t rowg = st + (uint32_t)(g * p.prow) + 4u * t;
       const uint32_t rowg8 = st + (uint32_t)((g + 8) * p.prow) + 4u * t;
-      const uint32_t sbase = st + (uint32_t)(kRows * p.prow);
-      const uint32_t zbase = sbase + (uint32_t)(kRows * p.sslice);
-      // Two independent MMA chains per set (first and second half of each chunk's k).
-      float acc[MSETS][4], tmp[MSETS][4], tmp2[MSETS][4];
+      const uint32_t sg_row = st + (uint32_t)(kRows * p.prow + g * p.sstride);
+      const uint32_t sg8_row = sg_row + (uint32_t)(8 * p.sstride);
+      const uint32_t zg_row = st + (uint32_t)(kRows * (p.prow + p.sstride) + g * p.zrow);
+      const uint32_t zg8_row = zg_row + (uint32_t)(8 * p.zrow);
+      float acc[MSETS][4];
 #pragma unroll
       for (int s = 0; s < MSETS; ++s)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[s][j] = tmp[s][j] = tmp2[s][j] = 0.0f;
-      int cur = -1;  // current group
-      uint32_t zlg = zl8, zhg = zh8, zlg8 = zl8, zhg8 = zh8;
-      float sg = 0.0f, sg8 = 0.0f;
-      auto flush = [&]() {
-#pragma unroll
-        for (int s = 0; s < MSETS; ++s) {
-          acc[s][0] = fmaf(tmp[s][0] + tmp2[s][0], sg, acc[s][0]);
-          acc[s][1] = fmaf(tmp[s][1] + tmp2[s][1], sg, acc[s][1]);
-          acc[s][2] = fmaf(tmp[s][2] + tmp2[s][2], sg8, acc[s][2]);
-          acc[s][3] = fmaf(tmp[s][3] + tmp2[s][3], sg8, acc[s][3]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) tmp[s][j] = tmp2[s][j] = 0.0f;
-        }
-      };
+        for (int j = 0; j < 4; ++j) acc[s][j] = 0.0f;
       if (ok) {
-        for (int c = c_lo; c < c_hi; ++c) {
-          const int grp = (k0 + c * 32) >> p.gshift;  // absolute group (zero points)
-          if (grp != cur) {
-            if (cur >= 0) flush();
-            cur = grp;
-            const int gl = grp - gb;                     // group within the staged scales
-            if (S16) {
-              sg = half_bits_to_float(lds_u16_a(sbase + (uint32_t)(g * p.sslice + 2 * gl)));
-              sg8 = half_bits_to_float(lds_u16_a(sbase + (uint32_t)((g + 8) * p.sslice + 2 * gl)));
-            } else {
-              sg = __uint_as_float(lds_u32_a(sbase + (uint32_t)(g * p.sslice + 4 * gl)));
-              sg8 = __uint_as_float(lds_u32_a(sbase + (uint32_t)((g + 8) * p.sslice + 4 * gl)));
-            }
-            if (ZP) {
-              const uint32_t sh = (uint32_t)(grp & 1) * 4u;
-              const uint32_t z0 = (lds_u8_a(zbase + (uint32_t)(g * p.zrow + (grp >> 1))) >> sh) & 15u;
-              const uint32_t z1 = (lds_u8_a(zbase + (uint32_t)((g + 8) * p.zrow + (grp >> 1))) >> sh) & 15u;
-              zlg = zp_lo_const(z0);
-              zhg = zp_hi_const(z0);
-              zlg8 = zp_lo_const(z1);
-              zhg8 = zp_hi_const(z1);
+        for (int q = q_lo; q < q_hi; ++q) {
+          // Group q of the slice: its scales (rows g and g + 8) and zero points.
+          float sg, sg8;
+          if (s16) {
+            sg = half_bits_to_float(lds_u16_a(sg_row + 2u * (uint32_t)q));
+            sg8 = half_bits_to_float(lds_u16_a(sg8_row + 2u * (uint32_t)q));
+          } else {
+            sg = __uint_as_float(lds_u32_a(sg_row + 4u * (uint32_t)q));
+            sg8 = __uint_as_float(lds_u32_a(sg8_row + 4u * (uint32_t)q));
+          }
+          uint32_t zlg = zl8, zhg = zh8, zlg8 = zl8, zhg8 = zh8;
+          if (ZP) {
+            const int grp = gb + q;  // zero points are staged as whole rows
+            const uint32_t sh = (uint32_t)(grp & 1) * 4u;
+            const uint32_t z0 = (lds_u8_a(zg_row + (uint32_t)(grp >> 1)) >> sh) & 15u;
+            const uint32_t z1 = (lds_u8_a(zg8_row + (uint32_t)(grp >> 1)) >> sh) & 15u;
+            zlg = zp_lo_const(z0);
+            zhg = zp_hi_const(z0);
+            zlg8 = zp_lo_const(z1);
+            zhg8 = zp_hi_const(z1);
+          }
+          // Fresh fp32 fragments for the group: chain 1 takes physical k = 8t + {0,4,1,5},
+          // chain 2 k = 8t + {2,6,3,7} of each chunk (one chain for single-chunk groups).
+          float tmp[MSETS][4], tmp2[MSETS][4];
+#pragma unroll
+          for (int cc = 0; cc < CPG; ++cc) {
+            const uint32_t c = (uint32_t)(q * CPG + cc);
+            const uint32_t wa = lds_u32_a(rowg + 16u * c);
+            const uint32_t wb = lds_u32_a(rowg8 + 16u * c);
+            uint32_t da[4], db[4];
+            nibbles_to_centered_half2(wa, zlg, zhg, da);
+            nibbles_to_centered_half2(wb, zlg8, zhg8, db);
+#pragma unroll
+            for (int s = 0; s < MSETS; ++s) {
+              uint4 xf = make_uint4(0, 0, 0, 0);
+              if (xlive[s]) xf = lds128_a(xlane + ((uint32_t)s * (uint32_t)C + c) * 512u);
+              if (CPG == 1) {
+                mma16816_zero(tmp[s], da[0], db[0], da[1], db[1], xf.x, xf.y);
+                mma16816(tmp[s], da[2], db[2], da[3], db[3], xf.z, xf.w);
+              } else if (cc == 0) {
+                mma16816_zero(tmp[s], da[0], db[0], da[1], db[1], xf.x, xf.y);
+                mma16816_zero(tmp2[s], da[2], db[2], da[3], db[3], xf.z, xf.w);
+              } else {
+                mma16816(tmp[s], da[0], db[0], da[1], db[1], xf.x, xf.y);
+                mma16816(tmp2[s], da[2], db[2], da[3], db[3], xf.z, xf.w);
+              }
             }
           }
-          const uint32_t wa = lds_u32_a(rowg + 16u * c);
-          const uint32_t wb = lds_u32_a(rowg8 + 16u * c);
-          uint32_t da[4], db[4];
-          nibbles_to_centered_half2(wa, zlg, zhg, da);
-          nibbles_to_centered_half2(wb, zlg8, zhg8, db);
 #pragma unroll
           for (int s = 0; s < MSETS; ++s) {
-            const uint4 xf = lds128_a(xs_u32 + (uint32_t)(((s * C + c) * 32 + lane) * 16));
-            mma16816(tmp[s], da[0], db[0], da[1], db[1], xf.x, xf.y);
-            mma16816(tmp2[s], da[2], db[2], da[3], db[3], xf.z, xf.w);
+            if (CPG > 1) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) tmp[s][j] += tmp2[s][j];
+            }
+            acc[s][0] = fmaf(tmp[s][0], sg, acc[s][0]);
+            acc[s][1] = fmaf(tmp[s][1], sg, acc[s][1]);
+            acc[s][2] = fmaf(tmp[s][2], sg8, acc[s][2]);
+            acc[s][3] = fmaf(tmp[s][3], sg8, acc[s][3]);
           }
         }
-        if (cur >= 0) flush();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[slot]);
@@ -277,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
       for (int s = 0; s < MSETS; ++s)
         *reinterpret_cast<float4*>(&red[gi][gw][s][lane][0]) = make_float4(acc[s][0], acc[s][1], acc[s][2], acc[s][3]);
       group_bar(gi);
-      // Fixed-order sum over the K slices; one thread per (row, m).
+      // Fixed-order sum over the warps' K ranges; one thread per (row, m).
       const int n0 = (t_begin + i) * kRows;
       if constexpr (F32) {
         for (int e = gw * 32 + lane; e < kRows * p.Mout; e += kGW * 32) {
@@ -289,22 +336,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
                 failed ? __uint_as_float(0x7fc00000u) : ldexpf(v, p.rexp[m]) + (p.biasf ? p.biasf[n] : 0.0f);
           }
         }
-        group_bar(gi);
-        continue;
-      }
-      for (int e = gw * 32 + lane; e < kRows * 8 * MSETS; e += kGW * 32) {
-        const int row = e % kRows, m = e / kRows;
-        const int s = m >> 3, mm = m & 7;
-        const int l = (row & 7) * 4 + (mm >> 1), j = ((row >> 3) << 1) + (mm & 1);
-        float v = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kGW; ++w) v += red[gi][w][s][l][j];
-        const int n = n0 + row;
-        if (m < p.M && n < p.N) {
-          if constexpr (SPLIT)
-            p.part[((long long)slice * p.M + m) * p.N + n] = failed ? __uint_as_float(0x7fc00000u) : v;
-          else
-            p.Y[(long long)m * p.N + n] = failed ? __ushort_as_half(0x7e00) : round_out(v, p.bias, n, p.bias_mode);
+      } else {
+        for (int e = gw * 32 + lane; e < kRows * 8 * MSETS; e += kGW * 32) {
+          const int row = e % kRows, m = e / kRows;
+          const float v = slice_sum<MSETS>(red[gi], row, m);
+          const int n = n0 + row;
+          if (m < p.M && n < p.N) {
+            if constexpr (SPLIT)
+              p.part[((long long)slice * p.M + m) * p.N + n] = failed ? __uint_as_float(0x7fc00000u) : v;
+            else
+              p.Y[(long long)m * p.N + n] = failed ? __ushort_as_half(0x7e00) : round_out(v, p.bias, n, p.bias_mode);
+          }
         }
       }
       group_bar(gi);
@@ -327,14 +369,25 @@ __global__ void __launch_bounds__(256) combine_slices_kernel(const float* __rest
 
 using SmKernel = void (*)(const SmArgs);
 
+template <int MSETS, int CPG, bool F32, bool SPLIT>
+SmKernel pick_zp(bool zp) {
+  return zp ? gemm_smallm_kernel<MSETS, CPG, true, F32, SPLIT> : gemm_smallm_kernel<MSETS, CPG, false, F32, SPLIT>;
+}
+
+// cpg: 32-k chunks per quant group (1, 2 or 4); anything else is not handled.
 template <int MSETS, bool F32, bool SPLIT = false>
-SmKernel pick(bool s16, bool zp) {
-  if (s16)
-    return zp ? gemm_smallm_kernel<MSETS, true, true, F32, SPLIT> : gemm_smallm_kernel<MSETS, true, false, F32, SPLIT>;
-  return zp ? gemm_smallm_kernel<MSETS, false, true, F32, SPLIT> : gemm_smallm_kernel<MSETS, false, false, F32, SPLIT>;
+SmKernel pick(int cpg, bool zp) {
+  if (cpg == 1) return pick_zp<MSETS, 1, F32, SPLIT>(zp);
+  if (cpg == 2) return pick_zp<MSETS, 2, F32, SPLIT>(zp);
+  if (cpg == 4) return pick_zp<MSETS, 4, F32, SPLIT>(zp);
+  return nullptr;
 }
 
 }  // namespace
+
+// Staged scale row stride for `bytes` of scales per row (a multiple of 16): congruent to 16
+// mod 32 bytes, so row r starts at bank 4 * (r * odd mod 8) and eight rows never collide.
+static int scale_stride(int bytes) { return bytes % 32 == 0 ? bytes + 16 : bytes; }
 
 // K-slice length for the small-M kernel: all of K when its rows, scales and activations fit
 // two ring slots, else the largest of 4096 / 2048 / 1024 (multiples of the block size) that
@@ -344,7 +397,7 @@ int smallm_kslice(int M, int K, int bs, int ssz, bool zp) {
   const int msets = M <= 8 ? 1 : 2;
   const int G = K / bs, zrow = zp ? (G + 1) / 2 : 0;
   auto fits = [&](int ks) {
-    const size_t stage = (size_t)kRows * (ks / 2 + kRowPad + (ks / bs) * ssz + zrow);
+    const size_t stage = (size_t)kRows * (ks / 2 + kRowPad + scale_stride((ks / bs) * ssz) + zrow);
     const size_t xbytes = (size_t)msets * (ks / 32) * 32 * 16;
     return xbytes + 2 * stage <= (size_t)kSmemBudget;
   };
@@ -368,7 +421,7 @@ namespace {
 cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
                                void* Y, int Mout, float* Yf, const float* biasf, const int* rexp,
                                void* workspace = nullptr, size_t ws_bytes = 0) {
-  if (M < 2 || M > 16 || bs < 32 || K % 32 != 0) return cudaErrorNotSupported;
+  if (M < 2 || M > 16 || (bs != 32 && bs != 64 && bs != 128) || K % 32 != 0) return cudaErrorNotSupported;
   SmArgs a = {};
   a.A = static_cast<const __half*>(A);
   a.packed = w.packed;
@@ -391,6 +444,7 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   a.nslices = (K + ks - 1) / ks;
   const int klast = K - (a.nslices - 1) * ks;
   a.sslice = (ks / bs) * a.ssz;
+  a.sstride = scale_stride(a.sslice);
   // Every bulk copy is a 16-byte multiple at a 16-byte offset: packed slices (k multiples
   // of 32), scale slices (checked here, also the last one, and the row stride) and a tile's
   // zero-point rows (16 * zrow bytes at a multiple of 16 * zrow: any zrow works for whole
@@ -405,7 +459,7 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
     a.part = static_cast<float*>(workspace);
   }
   a.prow = ks / 2 + kRowPad;
-  a.stage_bytes = kRows * (a.prow + a.sslice + a.zrow);
+  a.stage_bytes = kRows * (a.prow + a.sstride + a.zrow);
   const int msets = M <= 8 ? 1 : 2;
   const size_t xbytes = (size_t)msets * (ks / 32) * 32 * 16;
   if ((size_t)kSmemBudget < xbytes + 2 * (size_t)a.stage_bytes) return cudaErrorNotSupported;
@@ -425,10 +479,12 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   a.rexp = rexp;
   const bool f32 = Yf != nullptr;
   const size_t smem = (size_t)a.stages * a.stage_bytes + xbytes;
-  const bool s16 = w.scales_f16 != 0, zp = w.zp != nullptr;
+  const bool zp = w.zp != nullptr;
+  const int cpg = bs / 32;
   const bool split = a.nslices > 1;  // fp32-output calls never split
-  SmKernel kern = msets == 1 ? (f32 ? pick<1, true>(s16, zp) : (split ? pick<1, false, true>(s16, zp) : pick<1, false>(s16, zp)))
-                             : (f32 ? pick<2, true>(s16, zp) : (split ? pick<2, false, true>(s16, zp) : pick<2, false>(s16, zp)));
+  SmKernel kern = msets == 1 ? (f32 ? pick<1, true>(cpg, zp) : (split ? pick<1, false, true>(cpg, zp) : pick<1, false>(cpg, zp)))
+                             : (f32 ? pick<2, true>(cpg, zp) : (split ? pick<2, false, true>(cpg, zp) : pick<2, false>(cpg, zp)));
+  if (kern == nullptr) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ctx.variant = f32 ? "gemm_smallm_mma16816_f32split" : "gemm_smallm_mma16816";

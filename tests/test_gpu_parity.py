@@ -180,6 +180,26 @@ def test_gemm_small_m_ragged(env, M, K, N, bs, sdt, zp):
     assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
 
 
+# Every block size the small-M kernel specialises on (1, 2 or 4 chunks of 32 k per group),
+# both scale dtypes, with and without zero points, fewer groups than K-splitting warps, and
+# partial last tiles.
+@pytest.mark.parametrize("M,K,N,bs,sdt,zp", [(2, 512, 64, 32, "f32", True), (6, 1536, 48, 64, "f32", False),
+                                             (11, 1024, 160, 128, "f16", False), (4, 512, 16, 128, "f32", True),
+                                             (16, 2048, 33, 32, "f16", True), (3, 4096, 40, 64, "f16", False),
+                                             (9, 640, 72, 32, "f32", False), (8, 3072, 32, 128, "f32", True)])
+def test_gemm_small_m_block_sizes(env, M, K, N, bs, sdt, zp):
+    mnb, torch, dev = env
+    wl = syn.custom(f"smb_{M}_{K}_{N}_{bs}_{sdt}_{zp}", M, K, N, bs, scales_dtype=sdt, has_zp=zp)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    y = mnb.mnb_gemm(upload_act(A, dev), *upload_weight(w, dev), K, N, bs)
+    assert mnb.mnb_last_variant() == "gemm_smallm_mma16816"
+    torch.cuda.synchronize()
+    mnb.mnb_check_device_status()
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
+    assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
+
+
 @pytest.mark.parametrize("M,K,N,bs,sdt,zp", [(256, 128, 128, 128, "f16", True),
                                              (17, 128, 130, 32, "f16", True),
                                              (64, 256, 256, 128, "f16", True),
