@@ -35,7 +35,7 @@ constexpr int kGW = kCW / kGroups;
 constexpr int kThreads = (kCW + 1) * 32;
 constexpr int kRowPad = 16;      // bytes between staged rows
 constexpr int kMaxStages = 4;
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 208 * 1024;  // dynamic; static shared memory is at most ~17 KB
 
 struct SmArgs {
   const __half* A;
@@ -59,6 +59,7 @@ struct SmArgs {
   int prow;          // staged row stride = kslice / 2 + kRowPad
   int stage_bytes;   // kRows * (prow + sstride + zrow) (16-aligned)
   int stages;
+  int xstride;       // two row sets: staged activation row stride (bytes)
   int ntiles, tiles_per_cta;
   uint32_t* status;
   const __half* bias;
@@ -86,6 +87,28 @@ __device__ __forceinline__ void group_bar(int gi) {
   asm volatile("bar.sync %0, %1;" ::"r"(2 + gi), "n"(kGW * 32) : "memory");
 }
 
+// Every thread of both CTAs of the pair; also orders the mbarrier inits before any
+// multicast copy that signals them.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// 1-D bulk copy into the same shared-memory offset of every CTA in `mask`, each of which
+// sees `bytes` complete on its own mbarrier at `bar`'s offset.
+__device__ __forceinline__ void bulk_g2s_multicast(void* dst_smem, const void* src_gmem, uint32_t bytes,
+                                                   uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_u32(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
 // Fixed-order sum over the K slices of the staged partials of activation row m, weight row
 // `row` of the tile.
 template <int MSETS>
@@ -110,11 +133,19 @@ __device__ __forceinline__ void mma16816_zero(float (&c)[4], uint32_t a0, uint32
 
 // CPG: 32-k chunks per quant group (block size 32, 64 or 128).  The scale dtype is a
 // runtime property (one uniform branch per group); zero points are a template flag.
+//
+// Two row sets (M > 8) run as CTA pairs: each CTA of the pair bulk-copies every other
+// activation row into both CTAs' shared memory (row stride 64 mod 128 bytes, so the two
+// rows a quarter-warp reads sit in different banks), halving the activation reads from
+// L2; lanes pair the halves after loading them.  One row set stages the fragment order
+// with plain loads.
 template <int MSETS, int CPG, bool ZP, bool F32 = false, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p) {
+  constexpr bool kPair = MSETS == 2;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
-  __shared__ float red[kGroups][kGW][MSETS][32][4];
+  __shared__ uint64_t x_bar;
+  __shared__ __align__(16) float red[kGroups][kGW][MSETS][32][4];  // float4 stores
   __shared__ int failed;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -124,12 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
   const int C = klen >> 5;                         // 32-k chunks in the slice
   const int gb = SPLIT ? (k0 >> p.gshift) : 0;     // first group of the slice
   const int S = p.stages;
-  // shared memory: [ring stages][activations in fragment order]
+  // shared memory: [ring stages][activations: fragment order (one row set) or rows (pairs)]
   uint8_t* ring = smem_raw;
   uint8_t* xs = smem_raw + (size_t)S * p.stage_bytes;
   const int t_begin = blockIdx.x * p.tiles_per_cta;
   const int t_end = min(p.ntiles, t_begin + p.tiles_per_cta);
-  const int ntile = t_end - t_begin;
+  const int ntile = max(0, t_end - t_begin);  // a pair's padding CTA has none
 
   if (tid == 0) {
     failed = 0;
@@ -137,9 +168,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kGW);
     }
+    if (kPair) mbar_init(&x_bar, 1);
     fence_mbar_init();
   }
-  __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
+  else __syncthreads();
+  bool x_issued = false, x_ok = true;
 
   if (warp == kCW) {
     // ------------------------------ producer ------------------------------------
@@ -181,47 +215,64 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
     pdl_launch_dependents();
     pdl_wait();
     const uint32_t xs_u32 = smem_u32(xs);
-    // Stage the activations once: entry (set s, chunk c, lane l = 4g + t) holds
-    // A[8s + g][k0 + 32c + 8t .. +8], paired (x0,x4)(x1,x5)(x2,x6)(x3,x7); rows m >= M are
-    // zero.  Warp w fills chunks w, w + kCW, ..., with up to kBatch loads per set in flight
-    // before the first store.
-    {
-      constexpr int kBatch = 8;
-      bool live[MSETS];
-      const __half* arow[MSETS];
-#pragma unroll
-      for (int s = 0; s < MSETS; ++s) {
-        const int m = 8 * s + (lane >> 2);
-        live[s] = m < p.M;
-        arow[s] = p.A + (long long)(live[s] ? m : 0) * p.K + k0 + 8 * (lane & 3);
+    if constexpr (kPair) {
+      // This CTA's activation rows (every other one) go to both CTAs of the pair.
+      if (warp == 0 && lane == 0) {
+        const int rank = (int)cluster_rank();
+        mbar_arrive_expect_tx(&x_bar, (uint32_t)(p.M * klen * 2));
+        for (int m = rank; m < p.M; m += 2)
+          bulk_g2s_multicast(xs + (size_t)m * p.xstride, p.A + (long long)m * p.K + k0, (uint32_t)(klen * 2),
+                             &x_bar, (uint16_t)0x3);
+        x_issued = true;
       }
-      for (int cb = warp; cb < C; cb += kBatch * kCW) {
-        uint4 x[MSETS][kBatch];
-#pragma unroll
-        for (int s = 0; s < MSETS; ++s)
-#pragma unroll
-          for (int u = 0; u < kBatch; ++u) {
-            const int c = cb + u * kCW;
-            x[s][u] = make_uint4(0, 0, 0, 0);
-            if (live[s] && c < C) x[s][u] = *reinterpret_cast<const uint4*>(arow[s] + 32 * c);
-          }
-#pragma unroll
-        for (int s = 0; s < MSETS; ++s)
-#pragma unroll
-          for (int u = 0; u < kBatch; ++u) {
-            const int c = cb + u * kCW;
-            if (c < C) {
-              uint32_t q[4];
-              pair_halves_stride4(x[s][u], q);
-              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
-                               xs_u32 + (uint32_t)(((s * C + c) * 32 + lane) * 16)),
-                           "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
-                           : "memory");
+      if (!mbar_wait_bounded(&x_bar, 0)) {
+        report_status(p.status, kStatusFullWait);
+        atomicExch(&failed, 1);
+        x_ok = false;
+      }
+    } else {
+      // Stage the activations once: entry (set s, chunk c, lane l = 4g + t) holds
+      // A[8s + g][k0 + 32c + 8t .. +8], paired (x0,x4)(x1,x5)(x2,x6)(x3,x7); rows m >= M are
+      // zero.  Warp w fills chunks w, w + kCW, ..., with up to kBatch loads per set in flight
+      // before the first store.
+      {
+        constexpr int kBatch = 8;
+        bool live[MSETS];
+        const __half* arow[MSETS];
+  #pragma unroll
+        for (int s = 0; s < MSETS; ++s) {
+          const int m = 8 * s + (lane >> 2);
+          live[s] = m < p.M;
+          arow[s] = p.A + (long long)(live[s] ? m : 0) * p.K + k0 + 8 * (lane & 3);
+        }
+        for (int cb = warp; cb < C; cb += kBatch * kCW) {
+          uint4 x[MSETS][kBatch];
+  #pragma unroll
+          for (int s = 0; s < MSETS; ++s)
+  #pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+              const int c = cb + u * kCW;
+              x[s][u] = make_uint4(0, 0, 0, 0);
+              if (live[s] && c < C) x[s][u] = *reinterpret_cast<const uint4*>(arow[s] + 32 * c);
             }
-          }
+  #pragma unroll
+          for (int s = 0; s < MSETS; ++s)
+  #pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+              const int c = cb + u * kCW;
+              if (c < C) {
+                uint32_t q[4];
+                pair_halves_stride4(x[s][u], q);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                                 xs_u32 + (uint32_t)(((s * C + c) * 32 + lane) * 16)),
+                             "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
+                             : "memory");
+              }
+            }
+        }
       }
+      consumer_bar();
     }
-    consumer_bar();
 
     const int g = lane >> 2, t = lane & 3;
     const int gi = warp / kGW, gw = warp % kGW;  // tile group, warp within it
@@ -233,9 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
     // Lanes whose activation row is past M hold zeros and skip the shared-memory read.
     const uint32_t xlane = xs_u32 + (uint32_t)lane * 16u;
     bool xlive[MSETS];
+    uint32_t xrow[MSETS];  // pair layout: this lane's 16 bytes of row 8s + g, chunk 0
 #pragma unroll
-    for (int s = 0; s < MSETS; ++s) xlive[s] = 8 * s + g < p.M;
-    bool ok = true;
+    for (int s = 0; s < MSETS; ++s) {
+      xlive[s] = 8 * s + g < p.M;
+      xrow[s] = xs_u32 + (uint32_t)((8 * s + g) * p.xstride) + 16u * (uint32_t)t;
+    }
+    bool ok = x_ok;
     for (int i = gi; i < ntile; i += kGroups) {
       const int slot = i % S;
       const uint32_t phase = (uint32_t)(i / S) & 1u;
@@ -292,7 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
 #pragma unroll
             for (int s = 0; s < MSETS; ++s) {
               uint4 xf = make_uint4(0, 0, 0, 0);
-              if (xlive[s]) xf = lds128_a(xlane + ((uint32_t)s * (uint32_t)C + c) * 512u);
+              if (xlive[s]) {
+                if constexpr (kPair) {
+                  uint32_t q[4];
+                  pair_halves_stride4(lds128_a(xrow[s] + 64u * c), q);
+                  xf = make_uint4(q[0], q[1], q[2], q[3]);
+                } else {
+                  xf = lds128_a(xlane + ((uint32_t)s * (uint32_t)C + c) * 512u);
+                }
+              }
               if (CPG == 1) {
                 mma16816_zero(tmp[s], da[0], db[0], da[1], db[1], xf.x, xf.y);
                 mma16816(tmp[s], da[2], db[2], da[3], db[3], xf.z, xf.w);
@@ -352,6 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
       group_bar(gi);
     }
   }
+  if constexpr (kPair) {
+    // Neither CTA of the pair leaves while a copy it issued may still land in the other.
+    if (x_issued && !x_ok) (void)mbar_wait_bounded(&x_bar, 0);
+    __syncwarp();
+    cluster_sync_all();
+  }
 }
 
 // Fixed-order sum of the split-K partials, then the fp16 epilogue (bias modes).
@@ -389,17 +458,25 @@ SmKernel pick(int cpg, bool zp) {
 // mod 32 bytes, so row r starts at bank 4 * (r * odd mod 8) and eight rows never collide.
 static int scale_stride(int bytes) { return bytes % 32 == 0 ? bytes + 16 : bytes; }
 
+// Activation row stride of the CTA-pair layout for a slice of ks k (2 * ks is a multiple of
+// 64): congruent to 64 mod 128 bytes.
+static int pair_x_stride(int ks) { return (2 * ks) % 128 == 0 ? 2 * ks + 64 : 2 * ks; }
+
+// Shared memory for the staged activations of a slice of ks k.
+static size_t x_bytes(int M, int ks) {
+  if (M <= 8) return (size_t)(ks / 32) * 32 * 16;  // fragment order, one row set
+  return (size_t)M * pair_x_stride(ks);
+}
+
 // K-slice length for the small-M kernel: all of K when its rows, scales and activations fit
 // two ring slots, else the largest of 4096 / 2048 / 1024 (multiples of the block size) that
 // fits.  ssz: bytes per scale; zp: zero points present.  0: not handled.
 int smallm_kslice(int M, int K, int bs, int ssz, bool zp) {
   if (M < 2 || M > 16 || bs < 32 || K % 32 != 0) return 0;
-  const int msets = M <= 8 ? 1 : 2;
   const int G = K / bs, zrow = zp ? (G + 1) / 2 : 0;
   auto fits = [&](int ks) {
     const size_t stage = (size_t)kRows * (ks / 2 + kRowPad + scale_stride((ks / bs) * ssz) + zrow);
-    const size_t xbytes = (size_t)msets * (ks / 32) * 32 * 16;
-    return xbytes + 2 * stage <= (size_t)kSmemBudget;
+    return x_bytes(M, ks) + 2 * stage <= (size_t)kSmemBudget;
   };
   if (fits(K)) return K;
   for (int ks : {4096, 2048, 1024})
@@ -461,7 +538,8 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   a.prow = ks / 2 + kRowPad;
   a.stage_bytes = kRows * (a.prow + a.sstride + a.zrow);
   const int msets = M <= 8 ? 1 : 2;
-  const size_t xbytes = (size_t)msets * (ks / 32) * 32 * 16;
+  const size_t xbytes = x_bytes(M, ks);
+  a.xstride = pair_x_stride(ks);
   if ((size_t)kSmemBudget < xbytes + 2 * (size_t)a.stage_bytes) return cudaErrorNotSupported;
   a.stages = (int)((kSmemBudget - xbytes) / a.stage_bytes);
   if (a.stages > kMaxStages) a.stages = kMaxStages;
@@ -469,7 +547,9 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   // Spread (tile, slice) units over the SMs: each slice gets num_sms / nslices CTAs.
   const int ctas_per_slice = ctx.num_sms / a.nslices > 0 ? ctx.num_sms / a.nslices : 1;
   a.tiles_per_cta = (a.ntiles + ctas_per_slice - 1) / ctas_per_slice;
-  const int grid = (a.ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta;
+  int grid = (a.ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta;
+  const unsigned cluster = msets == 2 ? 2u : 1u;  // two row sets run as CTA pairs
+  grid = (grid + (int)cluster - 1) / (int)cluster * (int)cluster;
   a.status = ctx.status;
   a.bias = static_cast<const __half*>(ctx.bias);
   a.bias_mode = ctx.bias_mode;
@@ -488,8 +568,12 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ctx.variant = f32 ? "gemm_smallm_mma16816_f32split" : "gemm_smallm_mma16816";
-  if (a.nslices == 1) return launch_kernel(ctx, kern, dim3(grid), dim3(kThreads), smem, a);
-  e = launch_kernel(ctx, kern, dim3(grid, a.nslices), dim3(kThreads), smem, a);
+  auto launch = [&](dim3 g) {
+    return cluster > 1 ? launch_kernel_clustered(ctx, kern, g, dim3(kThreads), smem, cluster, a)
+                       : launch_kernel(ctx, kern, g, dim3(kThreads), smem, a);
+  };
+  if (a.nslices == 1) return launch(dim3(grid));
+  e = launch(dim3(grid, a.nslices));
   if (e != cudaSuccess) return e;
   const long long mn = (long long)M * N;
   const long long blocks = (mn + 255) / 256, cap = (long long)ctx.num_sms * 8;
