@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -515,6 +516,9 @@ def main():
     ap.add_argument("--impl", default="mnb", choices=["mnb", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline only, short CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log", default=None,
+                    help="keep the nvidia-smi clock samples of the timed regions in this CSV "
+                         "(default: a temporary file; the JSON line carries their summary)")
     ap.add_argument("--workload", default=None,
                     help="time one workload only (attn, gate_up, down, verify_m2/4/8/16 [_rot: activations rotated "
                          "with the weights], prefill, mlp_chain, "
@@ -545,8 +549,12 @@ def main():
     peaks, peak_src = load_peaks()
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") if rank == 0 else None)
+    clock_path = None
+    if rank == 0:
+        clock_path = args.clock_log or os.path.join(tempfile.gettempdir(), f"mnb_bench_clocks_{os.getpid()}.csv")
+        if os.path.dirname(clock_path):
+            os.makedirs(os.path.dirname(clock_path), exist_ok=True)
+    sampler = ClockSampler(local, clock_path)
     db = DeviceBench(torch, mnb, dev, l2, rank)
     sampler.start()
 

@@ -287,7 +287,8 @@ MNB_API mnb_status mnb_gemm_act_order(const void *A, int M, mnb_weight w, const 
  * mnb_gemm_act_order without a workspace, for callers that cannot allocate device
  * memory (a plugin inside a host framework that owns all device memory and hands it no
  * workspace, or a loop where cudaMalloc's implicit synchronisation is not allowed). The
- * paper has no counterpart: this entry point is this library's own.
+ * published MatMulNBits descriptions have no counterpart: this entry point is this
+ * library's own.
  * Same arguments and result as mnb_gemm_act_order minus workspace/ws_bytes. The
  * gathered activation (M * K' * 2 bytes) lives in a static device array of 8 MiB
  * (8388608 bytes) inside the library, held on every GPU that loads the library until

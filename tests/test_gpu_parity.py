@@ -323,6 +323,54 @@ def test_graph_capture_replay_matches_eager(env):
     assert torch.equal(y1, e1) and torch.equal(y4, e4)
 
 
+def test_small_m_pairs_graph_and_programmatic_launch(env):
+    """M > 8 runs as CTA pairs in a clustered launch: a chain of M = 16 GEMMs (each reading
+    the previous output) gives the eager bits with programmatic dependent launch and when
+    captured in a graph with it."""
+    mnb, torch, dev = env
+    wl = syn.WORKLOADS["verify_m16_k4096_n4096"]
+    ws = [upload_weight(syn.make_weight(wl, f"pairs{i}"), dev) for i in range(3)]
+    a = upload_act(syn.make_activation(wl), dev)
+
+    def chain():
+        x, outs = a, []
+        for w in ws:
+            x = mnb.mnb_gemm(x, *w, wl.K, wl.N, wl.block_size)
+            outs.append(x)
+        torch.cuda.synchronize()
+        return [o.clone() for o in outs]
+
+    eager = chain()
+    assert mnb.mnb_last_variant() == "gemm_smallm_mma16816"
+    mnb.mnb_set_programmatic_launch(True)
+    try:
+        pdl = chain()
+    finally:
+        mnb.mnb_set_programmatic_launch(False)
+    assert all(torch.equal(x, y) for x, y in zip(pdl, eager))
+    ys = [torch.empty_like(e) for e in eager]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    mnb.mnb_set_programmatic_launch(True)
+    try:
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                x = a
+                for w, y in zip(ws, ys):
+                    mnb.mnb_gemm(x, *w, wl.K, wl.N, wl.block_size, out=y)
+                    x = y
+    finally:
+        mnb.mnb_set_programmatic_launch(False)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    mnb.mnb_check_device_status()
+    assert all(torch.equal(x, y) for x, y in zip(ys, eager))
+    assert all(bool(torch.isfinite(e).all()) for e in eager)
+
+
 def test_repack_is_refused_during_capture(env):
     mnb, torch, dev = env
     K, N, bs = 256, 128, 32
