@@ -34,7 +34,7 @@ constexpr int kGroups = 2;       // tiles worked on at once (8 warps each)
 constexpr int kGW = kCW / kGroups;
 constexpr int kThreads = (kCW + 1) * 32;
 constexpr int kRowPad = 16;      // bytes between staged rows
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 208 * 1024;  // dynamic; static shared memory is at most ~17 KB
 
 struct SmArgs {
@@ -137,7 +137,7 @@ __device__ __forceinline__ void mma16816_zero(float (&c)[4], uint32_t a0, uint32
 // Two row sets (M > 8) run as CTA pairs: each CTA of the pair bulk-copies every other
 // activation row into both CTAs' shared memory (row stride 64 mod 128 bytes, so the two
 // rows a quarter-warp reads sit in different banks), halving the activation reads from
-// L2; lanes pair the halves after loading them.  One row set stages the fragment order
+// L2; lanes pair the halves after loading them.  One row set stages the fragment order,
 // with plain loads.
 template <int MSETS, int CPG, bool ZP, bool F32 = false, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p) {
@@ -231,44 +231,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
         x_ok = false;
       }
     } else {
-      // Stage the activations once: entry (set s, chunk c, lane l = 4g + t) holds
-      // A[8s + g][k0 + 32c + 8t .. +8], paired (x0,x4)(x1,x5)(x2,x6)(x3,x7); rows m >= M are
-      // zero.  Warp w fills chunks w, w + kCW, ..., with up to kBatch loads per set in flight
-      // before the first store.
+      // Stage the activations once, compactly: entry (chunk c, row m < M, quarter t) holds
+      // A[m][k0 + 32c + 8t .. +8], paired (x0,x4)(x1,x5)(x2,x6)(x3,x7), at byte
+      // ((c M + m) 4 + t) 16, so lane 4g + t finds row g of chunk c at 16 lane + 64 M c.
+      // Thread i fills quarter-chunks j = i, i + 512, ... of every row, all rows' loads in
+      // flight before the first store.
       {
-        constexpr int kBatch = 8;
-        bool live[MSETS];
-        const __half* arow[MSETS];
-  #pragma unroll
-        for (int s = 0; s < MSETS; ++s) {
-          const int m = 8 * s + (lane >> 2);
-          live[s] = m < p.M;
-          arow[s] = p.A + (long long)(live[s] ? m : 0) * p.K + k0 + 8 * (lane & 3);
-        }
-        for (int cb = warp; cb < C; cb += kBatch * kCW) {
-          uint4 x[MSETS][kBatch];
-  #pragma unroll
-          for (int s = 0; s < MSETS; ++s)
-  #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-              const int c = cb + u * kCW;
-              x[s][u] = make_uint4(0, 0, 0, 0);
-              if (live[s] && c < C) x[s][u] = *reinterpret_cast<const uint4*>(arow[s] + 32 * c);
+        const int J = 4 * C;  // quarter-chunks (8 halves) per row
+        for (int j = tid; j < J; j += kCW * 32) {
+          uint4 x[8];
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            x[m] = make_uint4(0, 0, 0, 0);
+            if (m < p.M) x[m] = *reinterpret_cast<const uint4*>(p.A + (long long)m * p.K + k0 + 8 * j);
+          }
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            if (m < p.M) {
+              uint32_t q[4];
+              pair_halves_stride4(x[m], q);
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                               xs_u32 + (uint32_t)((((j >> 2) * p.M + m) * 4 + (j & 3)) * 16)),
+                           "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
+                           : "memory");
             }
-  #pragma unroll
-          for (int s = 0; s < MSETS; ++s)
-  #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-              const int c = cb + u * kCW;
-              if (c < C) {
-                uint32_t q[4];
-                pair_halves_stride4(x[s][u], q);
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
-                                 xs_u32 + (uint32_t)(((s * C + c) * 32 + lane) * 16)),
-                             "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
-                             : "memory");
-              }
-            }
+          }
         }
       }
       consumer_bar();
@@ -280,9 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
     const int q_lo = (gw * Gs) / kGW, q_hi = ((gw + 1) * Gs) / kGW;  // this warp's groups
     const bool s16 = p.ssz == 2;
     const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
-    // Per chunk, this lane's activation fragments sit 512 bytes apart; per set, C * 512.
+    // One row set: this lane's activation fragment of chunk c sits at 16 lane + 64 M c.
     // Lanes whose activation row is past M hold zeros and skip the shared-memory read.
     const uint32_t xlane = xs_u32 + (uint32_t)lane * 16u;
+    const uint32_t xcstride = 64u * (uint32_t)p.M;
     bool xlive[MSETS];
     uint32_t xrow[MSETS];  // pair layout: this lane's 16 bytes of row 8s + g, chunk 0
 #pragma unroll
@@ -353,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
                   pair_halves_stride4(lds128_a(xrow[s] + 64u * c), q);
                   xf = make_uint4(q[0], q[1], q[2], q[3]);
                 } else {
-                  xf = lds128_a(xlane + ((uint32_t)s * (uint32_t)C + c) * 512u);
+                  xf = lds128_a(xlane + c * xcstride);
                 }
               }
               if (CPG == 1) {
@@ -464,7 +452,7 @@ static int pair_x_stride(int ks) { return (2 * ks) % 128 == 0 ? 2 * ks + 64 : 2 
 
 // Shared memory for the staged activations of a slice of ks k.
 static size_t x_bytes(int M, int ks) {
-  if (M <= 8) return (size_t)(ks / 32) * 32 * 16;  // fragment order, one row set
+  if (M <= 8) return (size_t)2 * M * ks;  // one row set, compact fragment order
   return (size_t)M * pair_x_stride(ks);
 }
 
