@@ -309,11 +309,11 @@ mnb_status mnb_gemv_gate_up_swiglu(const void* A, mnb_weight gate, mnb_weight up
 extern "C" {
 
 size_t mnb_workspace_bytes_f32(int M, int K, int N, int block_size) {
-  (void)N;
-  (void)block_size;
-  if (M < 2 || M > kMaxM || K < 1 || K > kMaxKN) return 0;
-  const size_t split = (size_t)4 * (size_t)M * (size_t)K;  // 2M fp16 rows of K
-  return split + ((size_t)4 * (size_t)M + 15) / 16 * 16;   // + M exponents
+  if (M < 2 || M > kMaxM || K < 1 || K > kMaxKN || N < 1 || N > kMaxKN) return 0;
+  const size_t split = (size_t)4 * (size_t)M * (size_t)K;           // 2M fp16 rows of K
+  size_t bytes = split + ((size_t)4 * (size_t)M + 15) / 16 * 16;    // + M exponents
+  if (2 * M <= 16) bytes += mnb::smallm_workspace_bytes(2 * M, K, N, block_size);  // + K-slice partials
+  return bytes;
 }
 
 mnb_status mnb_gemm_f32(const float* A, int M, mnb_weight w, const uint8_t* repacked, int K, int N, int block_size,
@@ -340,10 +340,12 @@ mnb_status mnb_gemm_f32(const float* A, int M, mnb_weight w, const uint8_t* repa
   } else {
     uint8_t* a2 = static_cast<uint8_t*>(workspace);
     int* rexp = reinterpret_cast<int*>(a2 + (size_t)4 * M * K);
+    const size_t head = (size_t)4 * M * K + ((size_t)4 * M + 15) / 16 * 16;
     e = mnb::launch_split_f32(ctx, A, M, K, a2, rexp);
     if (e == cudaSuccess) {
       if (2 * M <= 16)
-        e = mnb::launch_gemm_smallm_f32split(ctx, a2, M, q, K, N, block_size, Y, bias, rexp);
+        e = mnb::launch_gemm_smallm_f32split(ctx, a2, M, q, K, N, block_size, Y, bias, rexp, a2 + head,
+                                             ws_bytes - head);
       else
         e = mnb::launch_gemm_tc_f32split(ctx, a2, M, q, repacked, K, N, block_size, Y, bias, rexp);
     }

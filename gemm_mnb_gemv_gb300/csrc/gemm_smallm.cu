@@ -424,6 +424,25 @@ __global__ void __launch_bounds__(256) combine_slices_kernel(const float* __rest
   }
 }
 
+// fp32 output of split activations, summed over the K slices in slice order:
+// Yf[m, n] = 2^rexp[m] * sum_s (part[s][2m][n] + part[s][2m + 1][n]) + biasf[n].
+__global__ void __launch_bounds__(256) combine_slices_f32_kernel(const float* __restrict__ part, int nslices,
+                                                                 int Mout, int N, float* __restrict__ Yf,
+                                                                 const float* biasf, const int* rexp) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const long long mn = (long long)Mout * N, rows = 2LL * Mout * N;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < mn; i += (long long)gridDim.x * blockDim.x) {
+    const int m = (int)(i / N), n = (int)(i % N);
+    float v = 0.0f;
+    for (int s = 0; s < nslices; ++s) {
+      const float* ps = part + s * rows + (long long)(2 * m) * N + n;
+      v += ps[0] + ps[N];
+    }
+    Yf[i] = ldexpf(v, rexp[m]) + (biasf ? biasf[n] : 0.0f);
+  }
+}
+
 using SmKernel = void (*)(const SmArgs);
 
 template <int MSETS, int CPG, bool F32, bool SPLIT>
@@ -518,8 +537,8 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
       (a.zrow % 16 != 0 && N % kRows != 0))
     return cudaErrorNotSupported;
   if (a.nslices > 1) {
-    // fp32-output (split activation) calls use one slice; more need the partials workspace.
-    if (Yf != nullptr) return cudaErrorNotSupported;
+    // More than one slice needs the partials workspace (for fp32 output: partials of the
+    // 2 * Mout split rows, combined with their exponents afterwards).
     if (workspace == nullptr || ws_bytes < (size_t)a.nslices * M * N * 4) return cudaErrorNotSupported;
     a.part = static_cast<float*>(workspace);
   }
@@ -549,9 +568,9 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   const size_t smem = (size_t)a.stages * a.stage_bytes + xbytes;
   const bool zp = w.zp != nullptr;
   const int cpg = bs / 32;
-  const bool split = a.nslices > 1;  // fp32-output calls never split
-  SmKernel kern = msets == 1 ? (f32 ? pick<1, true>(cpg, zp) : (split ? pick<1, false, true>(cpg, zp) : pick<1, false>(cpg, zp)))
-                             : (f32 ? pick<2, true>(cpg, zp) : (split ? pick<2, false, true>(cpg, zp) : pick<2, false>(cpg, zp)));
+  const bool split = a.nslices > 1;  // split calls write plain partials, fp32 output or not
+  SmKernel kern = msets == 1 ? (split ? pick<1, false, true>(cpg, zp) : (f32 ? pick<1, true>(cpg, zp) : pick<1, false>(cpg, zp)))
+                             : (split ? pick<2, false, true>(cpg, zp) : (f32 ? pick<2, true>(cpg, zp) : pick<2, false>(cpg, zp)));
   if (kern == nullptr) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -563,6 +582,13 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   if (a.nslices == 1) return launch(dim3(grid));
   e = launch(dim3(grid, a.nslices));
   if (e != cudaSuccess) return e;
+  if (f32) {
+    const long long mn = (long long)Mout * N;
+    const long long blocks = (mn + 255) / 256, cap = (long long)ctx.num_sms * 8;
+    ctx.variant = "gemm_smallm_mma16816_f32split_splitk";
+    return launch_kernel(ctx, combine_slices_f32_kernel, dim3((unsigned)(blocks < cap ? blocks : cap)), dim3(256), 0,
+                         static_cast<const float*>(a.part), a.nslices, Mout, N, Yf, biasf, rexp);
+  }
   const long long mn = (long long)M * N;
   const long long blocks = (mn + 255) / 256, cap = (long long)ctx.num_sms * 8;
   ctx.variant = "gemm_smallm_mma16816_splitk";
@@ -579,9 +605,10 @@ cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeig
 }
 
 cudaError_t launch_gemm_smallm_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w, int K, int N,
-                                        int bs, float* Y, const float* bias, const int* rexp) {
+                                        int bs, float* Y, const float* bias, const int* rexp, void* workspace,
+                                        size_t ws_bytes) {
   if (M < 1 || 2 * M > 16) return cudaErrorNotSupported;
-  return launch_smallm_impl(ctx, A2, 2 * M, w, K, N, bs, nullptr, M, Y, bias, rexp);
+  return launch_smallm_impl(ctx, A2, 2 * M, w, K, N, bs, nullptr, M, Y, bias, rexp, workspace, ws_bytes);
 }
 
 }  // namespace mnb

@@ -68,7 +68,8 @@ cudaError_t launch_gemv_f32_tma(LaunchCtx& ctx, const float* A, const QWeight& w
                                 float* Y, const float* bias);
 cudaError_t launch_split_f32(LaunchCtx& ctx, const float* A, int M, int K, void* A2, int* rexp);
 cudaError_t launch_gemm_smallm_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w, int K, int N,
-                                        int bs, float* Y, const float* bias, const int* rexp);
+                                        int bs, float* Y, const float* bias, const int* rexp,
+                                        void* workspace = nullptr, size_t ws_bytes = 0);
 cudaError_t launch_gemm_tc_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w,
                                     const uint8_t* repacked, int K, int N, int bs, float* Y, const float* bias,
                                     const int* rexp);

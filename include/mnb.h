@@ -186,14 +186,19 @@ MNB_API mnb_status mnb_gemv_gate_up_swiglu(const void *A, mnb_weight gate, mnb_w
  * outputs in that row.
  */
 
-/* Workspace bytes mnb_gemm_f32 needs: 0 for M = 1, else 4*M*K + 4*M rounded up to 16. */
+/*
+ * Workspace bytes mnb_gemm_f32 needs: 0 for M = 1, else 4*M*K (the split activation) +
+ * 4*M rounded up to 16 (row exponents), plus for 2 <= M <= 8 with K beyond one
+ * shared-memory pass the fp32 K-slice partials of the 2*M split rows
+ * (mnb_workspace_bytes(2*M, K, N, block_size) bytes).
+ */
 MNB_API size_t mnb_workspace_bytes_f32(int M, int K, int N, int block_size);
 
 /*
  * fp32 Y[M, N] = A[M, K] . dequant(B)^T (+ bias[n] when bias is not NULL). Weight
  * arguments as mnb_gemm; `repacked` (mnb_repack) is required when M > 8, because the
  * split activation then has more than 16 rows and runs on the tcgen05 kernel. The
- * workspace holds the split activation and the row exponents; its contents need no
+ * workspace holds the split activation, the row exponents and any K-slice partials; its contents need no
  * initialisation and are overwritten by each call, so calls sharing one workspace must
  * be ordered on one stream.
  */

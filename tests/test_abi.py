@@ -62,6 +62,22 @@ def test_workspace_bytes_is_defined(lib):
         assert mnb.mnb_workspace_bytes(M, 4096, 4096, 64) >= 0
 
 
+def test_workspace_bytes_f32_layout(lib):
+    """fp32 workspace = split activation (4 M K) + exponents (4 M, rounded to 16) + the
+    K-slice partials of the 2 M split rows when those run on the small-M kernel."""
+    import gemm_mnb_gemv_gb300 as mnb
+    assert mnb.mnb_workspace_bytes_f32(1, 4096, 4096, 32) == 0
+    for M, K, N, bs in [(2, 4096, 4096, 64), (4, 14336, 256, 32), (8, 12288, 96, 128), (9, 4096, 512, 32),
+                        (300, 1024, 200, 32)]:
+        head = 4 * M * K + (4 * M + 15) // 16 * 16
+        part = mnb.mnb_workspace_bytes(2 * M, K, N, bs) if 2 * M <= 16 else 0
+        assert mnb.mnb_workspace_bytes_f32(M, K, N, bs) == head + part
+    # one shared-memory pass: no partials; K well beyond it: partials of every slice
+    assert mnb.mnb_workspace_bytes(8, 4096, 4096, 64) == 0
+    assert mnb.mnb_workspace_bytes(8, 14336, 256, 32) % (8 * 256 * 4) == 0
+    assert mnb.mnb_workspace_bytes(8, 14336, 256, 32) >= 2 * 8 * 256 * 4
+
+
 def _w(packed=16, scales=16, dtype=0, zp=None):
     import gemm_mnb_gemv_gb300 as mnb
     return mnb.MnbWeight(packed, scales, dtype, zp)

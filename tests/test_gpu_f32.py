@@ -53,6 +53,10 @@ F32_CASES = [
     ("f32_m40_wide", 40, 2048, 384, 128, "f32", True, "wide", False, "gemm_tcgen05_w128xa256_f32split"),
     ("f32_m300", 300, 1024, 200, 32, "f16", False, "normal", True, "gemm_tcgen05_w128xa256_f32split"),
     ("f32_m33_n96", 33, 512, 96, 32, "f16", True, "normal", True, "gemm_tcgen05_w128xa256_f32split"),
+    # K beyond one shared-memory pass: K-slice partials of the split rows, then the combine
+    ("f32_m4_k14336", 4, 14336, 256, 32, "f32", False, "normal", True, "gemm_smallm_mma16816_f32split_splitk"),
+    ("f32_m2_k12288_wide", 2, 12288, 144, 128, "f16", True, "wide", False, "gemm_smallm_mma16816_f32split_splitk"),
+    ("f32_m7_k8192", 7, 8192, 96, 64, "f32", True, "normal", True, "gemm_smallm_mma16816_f32split_splitk"),
 ]
 
 
