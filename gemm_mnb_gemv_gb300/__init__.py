@@ -393,7 +393,10 @@ def mnb_gemm_act_order(A, packed, scales, zero_points, perm, K: int, K_prepared:
     M = A.numel() // K
     w = _weight(packed, scales, zero_points)
     if workspace is None:
-        workspace = torch.empty(mnb_act_order_workspace_bytes(M, K_prepared), dtype=torch.uint8, device=A.device)
+        # the gathered activation, then room for the small-M kernel's K-slice partials
+        head = (mnb_act_order_workspace_bytes(M, K_prepared) + 15) // 16 * 16
+        workspace = torch.empty(head + mnb_workspace_bytes(M, K_prepared, N, block_size), dtype=torch.uint8,
+                                device=A.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=A.device)

@@ -508,7 +508,13 @@ mnb_status mnb_gemm_act_order(const void* A, int M, mnb_weight w, const uint8_t*
                          : cudaErrorNotSupported;
   if (e == cudaErrorNotSupported) {
     e = mnb::launch_act_order_gather(ctx, A, M, K, perm, K_prepared, workspace);
-    if (e == cudaSuccess) e = dispatch_gemm(ctx, workspace, M, q, repacked, K_prepared, N, block_size, Y);
+    // Workspace beyond the gathered activation (rounded to 16 bytes) serves the small-M
+    // kernel's K-slice partials when K' exceeds one shared-memory pass.
+    const size_t head = (need + 15) / 16 * 16;
+    void* rest = ws_bytes > head ? static_cast<uint8_t*>(workspace) + head : nullptr;
+    if (e == cudaSuccess)
+      e = dispatch_gemm(ctx, workspace, M, q, repacked, K_prepared, N, block_size, Y, rest,
+                        rest ? ws_bytes - head : 0);
   }
   return finish(fn, e, ctx);
 }
@@ -590,7 +596,11 @@ mnb_status mnb_gemm_act_order_noalloc(const void* A, int M, mnb_weight w, const 
                          : cudaErrorNotSupported;
   if (e == cudaErrorNotSupported) {
     e = mnb::launch_act_order_gather(ctx, A, M, K, perm, K_prepared, scratch);
-    if (e == cudaSuccess) e = dispatch_gemm(ctx, scratch, M, q, repacked, K_prepared, N, block_size, Y);
+    // The rest of the scratch serves the small-M kernel's K-slice partials.
+    const size_t head = (need + 15) / 16 * 16;
+    if (e == cudaSuccess)
+      e = dispatch_gemm(ctx, scratch, M, q, repacked, K_prepared, N, block_size, Y,
+                        static_cast<uint8_t*>(scratch) + head, kNoAllocScratchBytes - head);
   }
   return finish(fn, e, ctx);
 }

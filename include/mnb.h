@@ -280,8 +280,12 @@ MNB_API size_t mnb_act_order_workspace_bytes(int M, int K_prepared);
  * needed for M > 16 as in mnb_gemm); perm is the device copy of the plan's perm. The call
  * gathers A into `workspace` (at least mnb_act_order_workspace_bytes(M, K') bytes,
  * contents need no initialisation, overwritten by each call) and then runs mnb_gemm's
- * kernel for (M, K', N) on it. Calls that share one workspace must be ordered on one
- * stream. Tolerance as mnb_gemm, with the bound taken over the g_idx weights.
+ * kernel for (M, K', N) on it. A workspace larger by at least
+ * mnb_workspace_bytes(M, K', N, block_size), placed after the gathered activation rounded
+ * up to 16 bytes, lets 2 <= M <= 16 with K' beyond one shared-memory pass run on the
+ * small-M kernel's K slices (without it those calls take the generic kernel). Calls that
+ * share one workspace must be ordered on one stream. Tolerance as mnb_gemm, with the bound
+ * taken over the g_idx weights.
  */
 MNB_API mnb_status mnb_gemm_act_order(const void *A, int M, mnb_weight w, const uint8_t *repacked,
                                       const int32_t *perm, int K, int K_prepared, int N, int block_size,

@@ -125,6 +125,9 @@ ACT_ORDER_CASES = [
     ("ao_small_uneven", 13, 1024, 200, 32, "f32", True, "uneven"),
     ("ao_tc_bal", 300, 1024, 384, 128, "f16", True, "act_order"),
     ("ao_tc_uneven", 77, 1024, 256, 64, "f16", False, "uneven"),
+    # K' beyond one shared-memory pass: K slices with partials after the gathered rows
+    ("ao_small_bigk", 4, 12288, 160, 64, "f16", True, "act_order"),
+    ("ao_small_bigk_pairs", 12, 8192, 96, 128, "f32", True, "act_order"),
 ]
 
 
@@ -149,6 +152,26 @@ def test_gemm_act_order_parity(env, name, M, K, N, bs, sdt, zp, kind):
         assert variant == "gemv_tma_ring", variant  # separate gather, then the GEMV
     if M > 16:
         assert variant == tc_variant(N), variant
+    if name.startswith("ao_small_bigk"):
+        assert variant == "gemm_smallm_mma16816_splitk", variant
+    mnb.mnb_check_device_status()
+
+
+def test_gemm_act_order_bigk_without_room_for_partials_still_correct(env):
+    """A workspace of exactly mnb_act_order_workspace_bytes: the K-sliced product has no
+    room for its partials and the call takes the generic kernel, with the same bound."""
+    mnb, torch, dev = env
+    wl = syn.custom("ao_bigk_tight", 3, 12288, 96, 64, scales_dtype="f16", has_zp=True)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    g_idx = syn.make_g_idx(wl, "act_order")
+    kp, perm, _, perm_d, (pk, sc, zpp) = _prepare(mnb, torch, dev, wl, w, g_idx)
+    ws = torch.empty(mnb.mnb_act_order_workspace_bytes(3, kp), dtype=torch.uint8, device=dev)
+    y = mnb.mnb_gemm_act_order(upload_act(A, dev), pk, sc, zpp, perm_d, wl.K, kp, wl.N, 64, workspace=ws)
+    torch.cuda.synchronize()
+    assert mnb.mnb_last_variant() == "generic"
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, 64, g_idx)
+    assert_within_bound(y.float().cpu().numpy(), Y, B, wl.name)
     mnb.mnb_check_device_status()
 
 
