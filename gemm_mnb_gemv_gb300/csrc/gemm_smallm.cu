@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
 
     const int g = lane >> 2, t = lane & 3;
     const int gi = warp / kGW, gw = warp % kGW;  // tile group, warp within it
-    const int Gs = C / CPG;                      // quant groups in the slice
+    const int Gs = CPG > 0 ? C / CPG : 2 * C;   // quant groups in the slice
     const int q_lo = (gw * Gs) / kGW, q_hi = ((gw + 1) * Gs) / kGW;  // this warp's groups
     const bool s16 = p.ssz == 2;
     const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
@@ -299,7 +299,72 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
       for (int s = 0; s < MSETS; ++s)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[s][j] = 0.0f;
+      if constexpr (CPG == 0) {
       if (ok) {
+        // Block size 16: chunk c holds groups 2c (the words of lanes t < 2) and 2c + 1
+        // (t >= 2).  Each lane converts with its own group's zero point; each MMA step runs
+        // twice with the activation fragment of the other group's lanes zeroed, so the
+        // two groups accumulate into separate fragments, each scaled after accumulation.
+        const bool lo_half = t < 2;
+        const int c_lo = (gw * C) / kGW, c_hi = ((gw + 1) * C) / kGW;
+        for (int c = c_lo; c < c_hi; ++c) {
+          float sa, sa8, sb, sb8;  // scales of groups 2c (a) and 2c + 1 (b), rows g and g + 8
+          if (s16) {
+            const uint32_t h = lds_u32_a(sg_row + 4u * (uint32_t)c), h8 = lds_u32_a(sg8_row + 4u * (uint32_t)c);
+            sa = half_bits_to_float(h & 0xffffu);
+            sb = half_bits_to_float(h >> 16);
+            sa8 = half_bits_to_float(h8 & 0xffffu);
+            sb8 = half_bits_to_float(h8 >> 16);
+          } else {
+            const uint2 f = lds_u64_a(sg_row + 8u * (uint32_t)c), f8 = lds_u64_a(sg8_row + 8u * (uint32_t)c);
+            sa = __uint_as_float(f.x);
+            sb = __uint_as_float(f.y);
+            sa8 = __uint_as_float(f8.x);
+            sb8 = __uint_as_float(f8.y);
+          }
+          uint32_t zl = zl8, zh = zh8, zl_8 = zl8, zh_8 = zh8;
+          if (ZP) {
+            // zero-point byte (gb + 2c) / 2 holds group 2c (low nibble) and 2c + 1 (high)
+            const uint32_t zb = (uint32_t)((gb >> 1) + c);
+            const uint32_t b0 = lds_u8_a(zg_row + zb), b1 = lds_u8_a(zg8_row + zb);
+            const uint32_t z0 = lo_half ? (b0 & 15u) : (b0 >> 4), z1 = lo_half ? (b1 & 15u) : (b1 >> 4);
+            zl = zp_lo_const(z0);
+            zh = zp_hi_const(z0);
+            zl_8 = zp_lo_const(z1);
+            zh_8 = zp_hi_const(z1);
+          }
+          const uint32_t wa = lds_u32_a(rowg + 16u * (uint32_t)c);
+          const uint32_t wb = lds_u32_a(rowg8 + 16u * (uint32_t)c);
+          uint32_t da[4], db[4];
+          nibbles_to_centered_half2(wa, zl, zh, da);
+          nibbles_to_centered_half2(wb, zl_8, zh_8, db);
+#pragma unroll
+          for (int s = 0; s < MSETS; ++s) {
+            uint4 xf = make_uint4(0, 0, 0, 0);
+            if (xlive[s]) {
+              if constexpr (kPair) {
+                uint32_t q[4];
+                pair_halves_stride4(lds128_a(xrow[s] + 64u * (uint32_t)c), q);
+                xf = make_uint4(q[0], q[1], q[2], q[3]);
+              } else {
+                xf = lds128_a(xlane + (uint32_t)c * xcstride);
+              }
+            }
+            const uint4 xa = lo_half ? xf : make_uint4(0, 0, 0, 0);
+            const uint4 xb = lo_half ? make_uint4(0, 0, 0, 0) : xf;
+            float ta[4], tb[4];
+            mma16816_zero(ta, da[0], db[0], da[1], db[1], xa.x, xa.y);
+            mma16816(ta, da[2], db[2], da[3], db[3], xa.z, xa.w);
+            mma16816_zero(tb, da[0], db[0], da[1], db[1], xb.x, xb.y);
+            mma16816(tb, da[2], db[2], da[3], db[3], xb.z, xb.w);
+            acc[s][0] = fmaf(tb[0], sb, fmaf(ta[0], sa, acc[s][0]));
+            acc[s][1] = fmaf(tb[1], sb, fmaf(ta[1], sa, acc[s][1]));
+            acc[s][2] = fmaf(tb[2], sb8, fmaf(ta[2], sa8, acc[s][2]));
+            acc[s][3] = fmaf(tb[3], sb8, fmaf(ta[3], sa8, acc[s][3]));
+          }
+        }
+      }
+      } else if (ok) {
         for (int q = q_lo; q < q_hi; ++q) {
           // Group q of the slice: its scales (rows g and g + 8) and zero points.
           float sg, sg8;
@@ -450,9 +515,11 @@ SmKernel pick_zp(bool zp) {
   return zp ? gemm_smallm_kernel<MSETS, CPG, true, F32, SPLIT> : gemm_smallm_kernel<MSETS, CPG, false, F32, SPLIT>;
 }
 
-// cpg: 32-k chunks per quant group (1, 2 or 4); anything else is not handled.
+// cpg: 32-k chunks per quant group (1, 2 or 4; 0 for block size 16, two groups per
+// chunk); anything else is not handled.
 template <int MSETS, bool F32, bool SPLIT = false>
 SmKernel pick(int cpg, bool zp) {
+  if (cpg == 0) return pick_zp<MSETS, 0, F32, SPLIT>(zp);
   if (cpg == 1) return pick_zp<MSETS, 1, F32, SPLIT>(zp);
   if (cpg == 2) return pick_zp<MSETS, 2, F32, SPLIT>(zp);
   if (cpg == 4) return pick_zp<MSETS, 4, F32, SPLIT>(zp);
@@ -479,7 +546,7 @@ static size_t x_bytes(int M, int ks) {
 // two ring slots, else the largest of 4096 / 2048 / 1024 (multiples of the block size) that
 // fits.  ssz: bytes per scale; zp: zero points present.  0: not handled.
 int smallm_kslice(int M, int K, int bs, int ssz, bool zp) {
-  if (M < 2 || M > 16 || bs < 32 || K % 32 != 0) return 0;
+  if (M < 2 || M > 16 || bs < 16 || K % 32 != 0) return 0;
   const int G = K / bs, zrow = zp ? (G + 1) / 2 : 0;
   auto fits = [&](int ks) {
     const size_t stage = (size_t)kRows * (ks / 2 + kRowPad + scale_stride((ks / bs) * ssz) + zrow);
@@ -505,7 +572,8 @@ namespace {
 cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
                                void* Y, int Mout, float* Yf, const float* biasf, const int* rexp,
                                void* workspace = nullptr, size_t ws_bytes = 0) {
-  if (M < 2 || M > 16 || (bs != 32 && bs != 64 && bs != 128) || K % 32 != 0) return cudaErrorNotSupported;
+  if (M < 2 || M > 16 || (bs != 16 && bs != 32 && bs != 64 && bs != 128) || K % 32 != 0)
+    return cudaErrorNotSupported;
   SmArgs a = {};
   a.A = static_cast<const __half*>(A);
   a.packed = w.packed;
@@ -567,7 +635,7 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   const bool f32 = Yf != nullptr;
   const size_t smem = (size_t)a.stages * a.stage_bytes + xbytes;
   const bool zp = w.zp != nullptr;
-  const int cpg = bs / 32;
+  const int cpg = bs / 32;  // 0 for block size 16
   const bool split = a.nslices > 1;  // split calls write plain partials, fp32 output or not
   SmKernel kern = msets == 1 ? (split ? pick<1, false, true>(cpg, zp) : (f32 ? pick<1, true>(cpg, zp) : pick<1, false>(cpg, zp)))
                              : (split ? pick<2, false, true>(cpg, zp) : (f32 ? pick<2, true>(cpg, zp) : pick<2, false>(cpg, zp)));

@@ -48,7 +48,7 @@ F32_CASES = [
     ("f32_m2", 2, 4096, 384, 64, "f16", True, "normal", False, "gemm_smallm_mma16816_f32split"),
     ("f32_m5_wide", 5, 2048, 200, 32, "f32", True, "wide", True, "gemm_smallm_mma16816_f32split"),
     ("f32_m8", 8, 1024, 130, 128, "f16", False, "normal", False, "gemm_smallm_mma16816_f32split"),
-    ("f32_m3_bs16", 3, 512, 64, 16, "f16", True, "normal", False, "generic_f32"),
+    ("f32_m3_bs16", 3, 512, 64, 16, "f16", True, "normal", False, "gemm_smallm_mma16816_f32split"),
     ("f32_m9", 9, 1024, 256, 64, "f16", True, "normal", True, "gemm_tcgen05_w128xa256_f32split"),
     ("f32_m40_wide", 40, 2048, 384, 128, "f32", True, "wide", False, "gemm_tcgen05_w128xa256_f32split"),
     ("f32_m300", 300, 1024, 200, 32, "f16", False, "normal", True, "gemm_tcgen05_w128xa256_f32split"),

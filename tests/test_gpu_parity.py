@@ -180,13 +180,17 @@ def test_gemm_small_m_ragged(env, M, K, N, bs, sdt, zp):
     assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
 
 
-# Every block size the small-M kernel specialises on (1, 2 or 4 chunks of 32 k per group),
+# Every block size the small-M kernel specialises on (1, 2 or 4 chunks of 32 k per group, or
+# two groups per chunk for block size 16),
 # both scale dtypes, with and without zero points, fewer groups than K-splitting warps, and
 # partial last tiles.
 @pytest.mark.parametrize("M,K,N,bs,sdt,zp", [(2, 512, 64, 32, "f32", True), (6, 1536, 48, 64, "f32", False),
                                              (11, 1024, 160, 128, "f16", False), (4, 512, 16, 128, "f32", True),
                                              (16, 2048, 33, 32, "f16", True), (3, 4096, 40, 64, "f16", False),
-                                             (9, 640, 72, 32, "f32", False), (8, 3072, 32, 128, "f32", True)])
+                                             (9, 640, 72, 32, "f32", False), (8, 3072, 32, 128, "f32", True),
+                                             # block size 16: two groups per 32-k chunk
+                                             (5, 1024, 129, 16, "f16", True), (12, 2048, 48, 16, "f32", False),
+                                             (2, 4096, 64, 16, "f32", True), (16, 512, 80, 16, "f16", True)])
 def test_gemm_small_m_block_sizes(env, M, K, N, bs, sdt, zp):
     mnb, torch, dev = env
     wl = syn.custom(f"smb_{M}_{K}_{N}_{bs}_{sdt}_{zp}", M, K, N, bs, scales_dtype=sdt, has_zp=zp)
@@ -544,6 +548,7 @@ SPLITK_CASES = [
     (13, 12288, 96, 128, "f32", True),
     (3, 14336, 144, 128, "f16", True),    # last slice 2048 of 4096; zero-point rows of 56 bytes
     (16, 10240, 64, 32, "f16", False),
+    (4, 16384, 64, 16, "f16", True),      # block size 16, four slices
 ]
 
 
