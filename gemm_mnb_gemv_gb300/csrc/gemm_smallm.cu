@@ -22,6 +22,7 @@
 // matmul_nbits_marlin_gemm_f16 of marlin_gemm.rs).  Staged scale rows are padded to a
 // stride of 16 mod 32 bytes so the eight rows a warp reads together sit in eight banks,
 // and lanes whose activation row is past M skip their activation reads.
+#include "mma_sync.cuh"
 #include "mnb_device.cuh"
 #include "mnb_internal.h"
 
@@ -72,14 +73,6 @@ struct SmArgs {
   const int* rexp;
 };
 
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");
 }
@@ -119,16 +112,6 @@ __device__ __forceinline__ float slice_sum(const float (&red)[kGW][MSETS][32][4]
 #pragma unroll
   for (int w = 0; w < kGW; ++w) v += red[w][s][l][j];
   return v;
-}
-
-// One m16n8k16 step: c (+)= A . B with the fragment registers of one 32-bit word pair.
-__device__ __forceinline__ void mma16816_zero(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-  const float z = 0.0f;
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
-      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
 }
 
 // CPG: 32-k chunks per quant group (block size 32, 64 or 128).  The scale dtype is a
@@ -177,38 +160,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
 
   if (warp == kCW) {
     // ------------------------------ producer ------------------------------------
-    if (lane == 0) {
-      int slot = 0, issued = 0;
-      uint32_t phase = 0;
-      for (int i = 0; i < ntile; ++i) {
-        if (issued >= S && !mbar_wait_bounded(&empty_bar[slot], phase ^ 1u)) {
-          report_status(p.status, kStatusEmptyWait);
-          atomicExch(&failed, 1);
-          break;
-        }
-        const int n0 = (t_begin + i) * kRows;
-        const int nr = min(kRows, p.N - n0);
-        uint8_t* st = ring + (size_t)slot * p.stage_bytes;
-        const int pbytes = klen >> 1, sbytes = (klen >> p.gshift) * p.ssz;
-        const uint32_t bytes = (uint32_t)nr * (pbytes + sbytes + p.zrow);
-        mbar_arrive_expect_tx(&full_bar[slot], bytes);
-        for (int r = 0; r < nr; ++r)
-          bulk_g2s(st + r * p.prow, p.packed + (long long)(n0 + r) * p.row_bytes + (k0 >> 1), pbytes,
-                   &full_bar[slot]);
-        for (int r = 0; r < nr; ++r)
-          bulk_g2s(st + kRows * p.prow + r * p.sstride, p.scales + (long long)(n0 + r) * p.srow + gb * p.ssz,
-                   sbytes, &full_bar[slot]);
-        if (ZP)
-          bulk_g2s(st + kRows * (p.prow + p.sstride), p.zp + (long long)n0 * p.zrow, nr * p.zrow, &full_bar[slot]);
-        ++issued;
-        if (++slot == S) {
-          slot = 0;
-          phase ^= 1u;
-        }
+    // Lane 0 waits for the slot and arms its barrier; then lane r issues row r's copies,
+    // so a tile's row copies go out as one warp instruction each.
+    int slot = 0, issued = 0;
+    uint32_t phase = 0;
+    for (int i = 0; i < ntile; ++i) {
+      int free_slot = 1;
+      if (lane == 0 && issued >= S && !mbar_wait_bounded(&empty_bar[slot], phase ^ 1u)) {
+        report_status(p.status, kStatusEmptyWait);
+        atomicExch(&failed, 1);
+        free_slot = 0;
       }
+      if (!__shfl_sync(0xffffffffu, free_slot, 0)) break;
+      const int n0 = (t_begin + i) * kRows;
+      const int nr = min(kRows, p.N - n0);
+      uint8_t* st = ring + (size_t)slot * p.stage_bytes;
+      const int pbytes = klen >> 1, sbytes = (klen >> p.gshift) * p.ssz;
+      if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)nr * (pbytes + sbytes + p.zrow));
+      __syncwarp();
+      if (lane < nr) {
+        bulk_g2s(st + lane * p.prow, p.packed + (long long)(n0 + lane) * p.row_bytes + (k0 >> 1), pbytes,
+                 &full_bar[slot]);
+        bulk_g2s(st + kRows * p.prow + lane * p.sstride,
+                 p.scales + (long long)(n0 + lane) * p.srow + gb * p.ssz, sbytes, &full_bar[slot]);
+      }
+      if (ZP && lane == 0)
+        bulk_g2s(st + kRows * (p.prow + p.sstride), p.zp + (long long)n0 * p.zrow, nr * p.zrow, &full_bar[slot]);
+      ++issued;
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    if (lane == 0)
       for (int i = issued > S ? issued - S : 0; i < issued; ++i)
         (void)mbar_wait_bounded(&full_bar[i % S], (uint32_t)(i / S) & 1u);
-    }
     pdl_launch_dependents();
   } else {
     // ------------------------------ consumers -----------------------------------
