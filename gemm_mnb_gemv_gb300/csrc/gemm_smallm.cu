@@ -22,9 +22,14 @@
 // matmul_nbits_marlin_gemm_f16 of marlin_gemm.rs).  Staged scale rows are padded to a
 // stride of 16 mod 32 bytes so the eight rows a warp reads together sit in eight banks,
 // and lanes whose activation row is past M skip their activation reads.
+#include <cuda.h>
+#include <cstring>
+#include <cudaTypedefs.h>
+
 #include "mma_sync.cuh"
 #include "mnb_device.cuh"
 #include "mnb_internal.h"
+#include "tcgen05.cuh"
 
 namespace mnb {
 namespace {
@@ -58,7 +63,13 @@ struct SmArgs {
   int sstride;       // staged scale row stride: sslice rounded up to 16 mod 32 bytes, so the
                      // eight rows a warp reads for one group fall in eight different banks
   int prow;          // staged row stride = kslice / 2 + kRowPad
-  int stage_bytes;   // kRows * (prow + sstride + zrow) (16-aligned)
+  int stage_bytes;   // one ring slot (a multiple of 1024 with tensor-copied scales)
+  // Stage layout: packed rows at poff, scales at soff, zero points at zoff.  With stma the
+  // scales arrive as nsb 2-D tensor copies of 16 rows x 128 bytes each (128-byte
+  // swizzle, 1024-aligned): byte b of row r of box i sits at i * 2048 + r * 128 +
+  // (b ^ 16 (r mod 8)); otherwise as one copy per row at stride sstride.
+  int stma, nsb;
+  int poff, soff, zoff;
   int stages;
   int xstride;       // two row sets: staged activation row stride (bytes)
   int ntiles, tiles_per_cta;
@@ -123,9 +134,10 @@ __device__ __forceinline__ float slice_sum(const float (&red)[kGW][MSETS][32][4]
 // L2; lanes pair the halves after loading them.  One row set stages the fragment order,
 // with plain loads.
 template <int MSETS, int CPG, bool ZP, bool F32 = false, bool SPLIT = false>
-__global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_smallm_kernel(const SmArgs p, const __grid_constant__ CUtensorMap tmap_s) {
   constexpr bool kPair = MSETS == 2;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
+  extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ uint64_t x_bar;
   __shared__ __align__(16) float red[kGroups][kGW][MSETS][32][4];  // float4 stores
@@ -139,8 +151,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
   const int gb = SPLIT ? (k0 >> p.gshift) : 0;     // first group of the slice
   const int S = p.stages;
   // shared memory: [ring stages][activations: fragment order (one row set) or rows (pairs)]
-  uint8_t* ring = smem_raw;
-  uint8_t* xs = smem_raw + (size_t)S * p.stage_bytes;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned slots
+  uint8_t* xs = ring + (size_t)S * p.stage_bytes;
   const int t_begin = blockIdx.x * p.tiles_per_cta;
   const int t_end = min(p.ntiles, t_begin + p.tiles_per_cta);
   const int ntile = max(0, t_end - t_begin);  // a pair's padding CTA has none
@@ -176,16 +189,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
       const int nr = min(kRows, p.N - n0);
       uint8_t* st = ring + (size_t)slot * p.stage_bytes;
       const int pbytes = klen >> 1, sbytes = (klen >> p.gshift) * p.ssz;
-      if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)nr * (pbytes + sbytes + p.zrow));
+      // A tensor box always lands (and counts) whole: 16 rows x 128 bytes, rows past N zero.
+      const int nboxes = sbytes >> 7;
+      const uint32_t bytes = (uint32_t)nr * (pbytes + p.zrow) + (p.stma ? (uint32_t)nboxes * 2048u : (uint32_t)(nr * sbytes));
+      if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], bytes);
       __syncwarp();
-      if (lane < nr) {
-        bulk_g2s(st + lane * p.prow, p.packed + (long long)(n0 + lane) * p.row_bytes + (k0 >> 1), pbytes,
+      if (lane < nr)
+        bulk_g2s(st + p.poff + lane * p.prow, p.packed + (long long)(n0 + lane) * p.row_bytes + (k0 >> 1), pbytes,
                  &full_bar[slot]);
-        bulk_g2s(st + kRows * p.prow + lane * p.sstride,
-                 p.scales + (long long)(n0 + lane) * p.srow + gb * p.ssz, sbytes, &full_bar[slot]);
+      if (p.stma) {
+        if (lane == 1)
+          for (int b = 0; b < nboxes; ++b)
+            tc::tma_load_2d(st + p.soff + b * 2048, &tmap_s, gb * p.ssz + b * 128, n0, &full_bar[slot]);
+      } else if (lane < nr) {
+        bulk_g2s(st + p.soff + lane * p.sstride, p.scales + (long long)(n0 + lane) * p.srow + gb * p.ssz, sbytes,
+                 &full_bar[slot]);
       }
       if (ZP && lane == 0)
-        bulk_g2s(st + kRows * (p.prow + p.sstride), p.zp + (long long)n0 * p.zrow, nr * p.zrow, &full_bar[slot]);
+        bulk_g2s(st + p.zoff, p.zp + (long long)n0 * p.zrow, nr * p.zrow, &full_bar[slot]);
       ++issued;
       if (++slot == S) {
         slot = 0;
@@ -274,11 +295,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
         ok = false;
       }
       const uint32_t st = smem_u32(ring + (size_t)slot * p.stage_bytes);
-      const uint32_t rowg = st + (uint32_t)(g * p.prow) + 4u * t;
-      const uint32_t rowg8 = st + (uint32_t)((g + 8) * p.prow) + 4u * t;
-      const uint32_t sg_row = st + (uint32_t)(kRows * p.prow + g * p.sstride);
-      const uint32_t sg8_row = sg_row + (uint32_t)(8 * p.sstride);
-      const uint32_t zg_row = st + (uint32_t)(kRows * (p.prow + p.sstride) + g * p.zrow);
+      const uint32_t rowg = st + (uint32_t)(p.poff + g * p.prow) + 4u * t;
+      const uint32_t rowg8 = rowg + (uint32_t)(8 * p.prow);
+      const uint32_t sbase = st + (uint32_t)p.soff;
+      const uint32_t sg_row = sbase + (uint32_t)(g * p.sstride);  // row-copied scales
+      // Shared-memory address of byte `off` of this lane's scale row g (row g + 8: + hi8).
+      const uint32_t hi8 = p.stma ? 1024u : (uint32_t)(8 * p.sstride);
+      auto scale_addr = [&](uint32_t off) -> uint32_t {
+        return p.stma ? sbase + (off >> 7) * 2048u + (uint32_t)g * 128u + ((off & 127u) ^ ((uint32_t)g << 4))
+                      : sg_row + off;
+      };
+      const uint32_t zg_row = st + (uint32_t)(p.zoff + g * p.zrow);
       const uint32_t zg8_row = zg_row + (uint32_t)(8 * p.zrow);
       float acc[MSETS][4];
 #pragma unroll
@@ -296,13 +323,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
         for (int c = c_lo; c < c_hi; ++c) {
           float sa, sa8, sb, sb8;  // scales of groups 2c (a) and 2c + 1 (b), rows g and g + 8
           if (s16) {
-            const uint32_t h = lds_u32_a(sg_row + 4u * (uint32_t)c), h8 = lds_u32_a(sg8_row + 4u * (uint32_t)c);
+            const uint32_t sa_ = scale_addr(4u * (uint32_t)c);
+            const uint32_t h = lds_u32_a(sa_), h8 = lds_u32_a(sa_ + hi8);
             sa = half_bits_to_float(h & 0xffffu);
             sb = half_bits_to_float(h >> 16);
             sa8 = half_bits_to_float(h8 & 0xffffu);
             sb8 = half_bits_to_float(h8 >> 16);
           } else {
-            const uint2 f = lds_u64_a(sg_row + 8u * (uint32_t)c), f8 = lds_u64_a(sg8_row + 8u * (uint32_t)c);
+            const uint32_t sa_ = scale_addr(8u * (uint32_t)c);
+            const uint2 f = lds_u64_a(sa_), f8 = lds_u64_a(sa_ + hi8);
             sa = __uint_as_float(f.x);
             sb = __uint_as_float(f.y);
             sa8 = __uint_as_float(f8.x);
@@ -355,11 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_kernel(const SmArgs p
           // Group q of the slice: its scales (rows g and g + 8) and zero points.
           float sg, sg8;
           if (s16) {
-            sg = half_bits_to_float(lds_u16_a(sg_row + 2u * (uint32_t)q));
-            sg8 = half_bits_to_float(lds_u16_a(sg8_row + 2u * (uint32_t)q));
+            const uint32_t sa_ = scale_addr(2u * (uint32_t)q);
+            sg = half_bits_to_float(lds_u16_a(sa_));
+            sg8 = half_bits_to_float(lds_u16_a(sa_ + hi8));
           } else {
-            sg = __uint_as_float(lds_u32_a(sg_row + 4u * (uint32_t)q));
-            sg8 = __uint_as_float(lds_u32_a(sg8_row + 4u * (uint32_t)q));
+            const uint32_t sa_ = scale_addr(4u * (uint32_t)q);
+            sg = __uint_as_float(lds_u32_a(sa_));
+            sg8 = __uint_as_float(lds_u32_a(sa_ + hi8));
           }
           uint32_t zlg = zl8, zhg = zh8, zlg8 = zl8, zhg8 = zh8;
           if (ZP) {
@@ -494,7 +525,7 @@ __global__ void __launch_bounds__(256) combine_slices_f32_kernel(const float* __
   }
 }
 
-using SmKernel = void (*)(const SmArgs);
+using SmKernel = void (*)(const SmArgs, const CUtensorMap);
 
 template <int MSETS, int CPG, bool F32, bool SPLIT>
 SmKernel pick_zp(bool zp) {
@@ -535,8 +566,9 @@ int smallm_kslice(int M, int K, int bs, int ssz, bool zp) {
   if (M < 2 || M > 16 || bs < 16 || K % 32 != 0) return 0;
   const int G = K / bs, zrow = zp ? (G + 1) / 2 : 0;
   auto fits = [&](int ks) {
-    const size_t stage = (size_t)kRows * (ks / 2 + kRowPad + scale_stride((ks / bs) * ssz) + zrow);
-    return x_bytes(M, ks) + 2 * stage <= (size_t)kSmemBudget;
+    // two ring slots (either scale layout, 1024-aligned) + activations + base alignment
+    const size_t stage = ((size_t)kRows * (ks / 2 + kRowPad + scale_stride((ks / bs) * ssz) + zrow) + 1023) / 1024 * 1024;
+    return x_bytes(M, ks) + 2 * stage + 1024 <= (size_t)kSmemBudget;
   };
   if (fits(K)) return K;
   for (int ks : {4096, 2048, 1024})
@@ -597,12 +629,41 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
     a.part = static_cast<float*>(workspace);
   }
   a.prow = ks / 2 + kRowPad;
-  a.stage_bytes = kRows * (a.prow + a.sstride + a.zrow);
+  // Scales by 128-byte tensor boxes when every slice's scale bytes are whole boxes (one
+  // copy per 2 KB instead of one per row), else one bulk copy per row.
+  CUtensorMap tmap_s;
+  memset(&tmap_s, 0, sizeof(tmap_s));
+  a.stma = 0;
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+  if (encode && a.sslice % 128 == 0 && ((klast / bs) * a.ssz) % 128 == 0) {
+    const cuuint64_t gdim[2] = {(cuuint64_t)a.srow, (cuuint64_t)N};
+    const cuuint64_t gstride[1] = {(cuuint64_t)a.srow};
+    const cuuint32_t box[2] = {128, (cuuint32_t)kRows};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w.scales), gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      a.stma = 1;
+  }
+  if (a.stma) {
+    a.nsb = a.sslice / 128;
+    a.soff = 0;
+    a.poff = a.nsb * 2048;
+    a.zoff = a.poff + kRows * a.prow;
+    a.stage_bytes = (a.zoff + kRows * a.zrow + 1023) / 1024 * 1024;
+  } else {
+    a.nsb = 0;
+    a.poff = 0;
+    a.soff = kRows * a.prow;
+    a.zoff = a.soff + kRows * a.sstride;
+    a.stage_bytes = a.zoff + kRows * a.zrow;
+  }
   const int msets = M <= 8 ? 1 : 2;
   const size_t xbytes = x_bytes(M, ks);
   a.xstride = pair_x_stride(ks);
-  if ((size_t)kSmemBudget < xbytes + 2 * (size_t)a.stage_bytes) return cudaErrorNotSupported;
-  a.stages = (int)((kSmemBudget - xbytes) / a.stage_bytes);
+  const size_t usable = (size_t)kSmemBudget - 1024;  // minus the base-alignment slack
+  if (usable < xbytes + 2 * (size_t)a.stage_bytes) return cudaErrorNotSupported;
+  a.stages = (int)((usable - xbytes) / a.stage_bytes);
   if (a.stages > kMaxStages) a.stages = kMaxStages;
   a.ntiles = (N + kRows - 1) / kRows;
   // Spread (tile, slice) units over the SMs: each slice gets num_sms / nslices CTAs.
@@ -619,7 +680,7 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   a.biasf = biasf;
   a.rexp = rexp;
   const bool f32 = Yf != nullptr;
-  const size_t smem = (size_t)a.stages * a.stage_bytes + xbytes;
+  const size_t smem = (size_t)a.stages * a.stage_bytes + xbytes + 1024;
   const bool zp = w.zp != nullptr;
   const int cpg = bs / 32;  // 0 for block size 16
   const bool split = a.nslices > 1;  // split calls write plain partials, fp32 output or not
@@ -630,8 +691,8 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   if (e != cudaSuccess) return e;
   ctx.variant = f32 ? "gemm_smallm_mma16816_f32split" : "gemm_smallm_mma16816";
   auto launch = [&](dim3 g) {
-    return cluster > 1 ? launch_kernel_clustered(ctx, kern, g, dim3(kThreads), smem, cluster, a)
-                       : launch_kernel(ctx, kern, g, dim3(kThreads), smem, a);
+    return cluster > 1 ? launch_kernel_clustered(ctx, kern, g, dim3(kThreads), smem, cluster, a, tmap_s)
+                       : launch_kernel(ctx, kern, g, dim3(kThreads), smem, a, tmap_s);
   };
   if (a.nslices == 1) return launch(dim3(grid));
   e = launch(dim3(grid, a.nslices));

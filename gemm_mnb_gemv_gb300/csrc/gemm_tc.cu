@@ -456,6 +456,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 size_t gemm_tc_smem_bytes() { return kSmemBytes; }
 
+void* tensor_map_encode_fn() { return reinterpret_cast<void*>(get_encode()); }
+
 namespace {
 
 cudaError_t launch_tc_impl(LaunchCtx& ctx, const void* A, int M, const QWeight& w, const uint8_t* repacked, int K,

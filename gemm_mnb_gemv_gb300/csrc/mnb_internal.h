@@ -40,6 +40,8 @@ cudaError_t launch_act_order_gather(LaunchCtx& ctx, const void* A, int M, int K,
 // K' <= 8192); cudaErrorNotSupported otherwise.
 cudaError_t launch_gemv_tma_gather(LaunchCtx& ctx, const void* A, const int32_t* perm, int Ka, const QWeight& w,
                                    int Kp, int N, int bs, void* Y);
+// The driver's cuTensorMapEncodeTiled (CUDA 12 ABI), or null when unavailable.
+void* tensor_map_encode_fn();
 // Bulk-copy ring GEMV (M = 1); cudaErrorNotSupported when rows are not 16-byte multiples.
 cudaError_t launch_gemv_tma(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs,
                             void* Y);
