@@ -2,14 +2,15 @@
 //
 // HBM-bound (each weight is used M <= 16 times), so every weight byte is read once and
 // the dequantised values never touch shared memory: a CTA owns tiles of 16 weight rows,
-// a producer lane streams each tile (packed rows with a 16-byte row pad so the fragment
-// loads are bank-conflict free, plus the tile's scales and zero points) into a shared-
-// memory ring with 1-D bulk copies, and sixteen consumer warps in two groups of eight
-// work on two tiles at once, the eight warps of a group splitting K.  A lane converts
-// one 32-bit word (8 nibbles) of row g and of row g+8 into exact fp16 (code - zp) and
-// feeds them to two mma.sync.m16n8k16 (fp32 accumulate) as the A operand; the
-// activations, staged once per CTA in a fragment-ordered layout, are the B operand
-// (8 rows of A per instruction, two instructions per step for M > 8).
+// a producer warp streams each tile into a shared-memory ring (packed rows by one bulk
+// copy per row, with a 16-byte row pad so the fragment loads are bank-conflict free;
+// scales as 128-byte-swizzled 2-D tensor boxes, or one bulk copy per row when a slice's
+// scales are not whole boxes; zero points as one copy), and sixteen consumer warps in two
+// groups of eight work on two tiles at once, the eight warps of a group splitting K.  A
+// lane converts one 32-bit word (8 nibbles) of row g and of row g+8 into exact fp16
+// (code - zp) and feeds them to two mma.sync.m16n8k16 (fp32 accumulate) as the A
+// operand; the activations, staged once per CTA, are the B operand (8 rows of A per
+// instruction, two instructions per step for M > 8).
 //
 // The k index inside each MMA is permuted the same way for both operands: lane
 // (g, t) supplies physical k = 8t + {0,4,1,5} to the first MMA and 8t + {2,6,3,7} to the
@@ -19,9 +20,10 @@
 // group, a template parameter): it reads the group's scale and zero point of its two rows
 // once, accumulates the group's MMAs into a fresh fp32 fragment and adds that fragment
 // times the group scale to the running sum (scale after accumulate, as in
-// matmul_nbits_marlin_gemm_f16 of marlin_gemm.rs).  Staged scale rows are padded to a
-// stride of 16 mod 32 bytes so the eight rows a warp reads together sit in eight banks,
-// and lanes whose activation row is past M skip their activation reads.
+// matmul_nbits_marlin_gemm_f16 of marlin_gemm.rs).  The eight scale rows a warp reads
+// together sit in eight banks (swizzled boxes, or row-copied rows at a stride of 16 mod
+// 32 bytes), and lanes whose activation row is past M skip their activation reads.  Block
+// size 16 puts two groups in a chunk (see the CPG == 0 branch).
 #include <cuda.h>
 #include <cstring>
 #include <cudaTypedefs.h>
