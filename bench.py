@@ -578,6 +578,10 @@ def main():
         for M in (2, 4, 8, 16):
             extras[f"verify_m{M}"] = db.gemm(syn.WORKLOADS[f"verify_m{M}_k4096_n4096"], 20, 3, sampler,
                                              calls=200, repacked=False, shared_act=True)
+        # latency against M (same K, N and storage as the verify shapes except bs 32 at M = 1):
+        # the pages' concern is a cliff from M = 1 to M = 2
+        extras["verify_over_m1"] = {f"M{M}": extras[f"verify_m{M}"]["us_per_call"] / head["us_per_call"]
+                                    for M in (2, 4, 8, 16)}
         extras["prefill"] = db.gemm(syn.WORKLOADS["prefill_m2048_k4096_n14336"], 10, 3, sampler,
                                     calls=9, repacked=True)
         extras["mlp_chain"] = db.mlp_chain(10, 3, sampler)
