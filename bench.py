@@ -614,7 +614,8 @@ def main():
                        "scales": wl.scales_dtype, "zero_points": wl.has_zp,
                        "calls_per_step": CALLS_PER_STEP, "launch": "CUDA graph, programmatic dependent launch",
                        "l2": f"inputs larger than L2: {head['copies']} weight copies rotated "
-                             f"({head['copies'] * weight_bytes(wl) / 1e6:.0f} MB > 3 x {l2 / 1e6:.0f} MB L2)",
+                             f"({head['copies'] * weight_bytes(wl) / 1e6:.0f} MB > 3 x {l2 / 1e6:.0f} MB L2); "
+                             "one 8 KB activation vector shared by all calls",
                        "parallelism": f"replicas x{world}"},
             "us_per_call": head["us_per_call"], "us_per_call_median": head["us_per_call_median"],
             "roofline": roof, "clocks": clocks, "e2e": e2e,
