@@ -204,9 +204,11 @@ mnb_status mnb_gemv(const void* A, mnb_weight w, int K, int N, int block_size, v
 }
 
 size_t mnb_workspace_bytes(int M, int K, int N, int block_size) {
-  // Only the small-M kernel with K split into slices (K beyond one shared-memory pass)
-  // needs scratch: its fp32 partials.
-  if (M < 2 || M > 16 || K < 1 || N < 1 || K > kMaxKN || N > kMaxKN) return 0;
+  // fp32 K-slice partials: required by the small-M kernel when K exceeds one shared-memory
+  // pass; for M > 16 the tensor-core kernel uses them, when given, to split K over the SMs
+  // for outputs with few tiles.
+  if (M < 2 || M > kMaxM || K < 1 || N < 1 || K > kMaxKN || N > kMaxKN) return 0;
+  if (M > 16) return mnb::gemm_tc_workspace_bytes(M, K, N, block_size);
   return mnb::smallm_workspace_bytes(M, K, N, block_size);
 }
 
@@ -223,7 +225,7 @@ cudaError_t dispatch_gemm(mnb::LaunchCtx& ctx, const void* A, int M, const mnb::
   if (M == 1) {
     e = run_gemv(ctx, A, q, K, N, bs, Y);
   } else if (M > 16) {
-    e = mnb::launch_gemm_tc(ctx, A, M, q, repacked, K, N, bs, Y);
+    e = mnb::launch_gemm_tc(ctx, A, M, q, repacked, K, N, bs, Y, workspace, ws_bytes);
     if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, bs, Y);
   } else {
     e = mnb::launch_gemm_smallm(ctx, A, M, q, K, N, bs, Y, workspace, ws_bytes);
@@ -249,10 +251,11 @@ mnb_status gemm_impl(const char* fn, const void* A, int M, mnb_weight w, const u
   if ((st = check_weight(fn, w, &q)) != MNB_OK) return st;
   if ((st = check_ptr(fn, "A", A)) != MNB_OK) return st;
   if ((st = check_ptr(fn, "Y", Y)) != MNB_OK) return st;
-  const size_t need = mnb_workspace_bytes(M, K, N, block_size);
+  // Required for 2 <= M <= 16; optional (a K split when it fits) for M > 16.
+  const size_t need = M <= 16 ? mnb_workspace_bytes(M, K, N, block_size) : 0;
   if (ws_bytes < need)
     return fail(MNB_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", fn, ws_bytes, need);
-  if (need > 0 && (st = check_ptr(fn, "workspace", workspace)) != MNB_OK) return st;
+  if ((need > 0 || (workspace && ws_bytes > 0)) && (st = check_ptr(fn, "workspace", workspace)) != MNB_OK) return st;
   if (M > 16) {
     if ((st = check_ptr(fn, "repacked", repacked)) != MNB_OK) return st;
   }
@@ -312,7 +315,10 @@ size_t mnb_workspace_bytes_f32(int M, int K, int N, int block_size) {
   if (M < 2 || M > kMaxM || K < 1 || K > kMaxKN || N < 1 || N > kMaxKN) return 0;
   const size_t split = (size_t)4 * (size_t)M * (size_t)K;           // 2M fp16 rows of K
   size_t bytes = split + ((size_t)4 * (size_t)M + 15) / 16 * 16;    // + M exponents
-  if (2 * M <= 16) bytes += mnb::smallm_workspace_bytes(2 * M, K, N, block_size);  // + K-slice partials
+  // + K-slice partials of the 2M split rows (required on the small-M kernel, optional on
+  // the tensor-core kernel)
+  bytes += 2 * M <= 16 ? mnb::smallm_workspace_bytes(2 * M, K, N, block_size)
+                       : mnb::gemm_tc_workspace_bytes(2 * M, K, N, block_size);
   return bytes;
 }
 
@@ -327,7 +333,10 @@ mnb_status mnb_gemm_f32(const float* A, int M, mnb_weight w, const uint8_t* repa
   if ((st = check_ptr(fn, "A", A)) != MNB_OK) return st;
   if ((st = check_ptr(fn, "Y", Y)) != MNB_OK) return st;
   if (bias && !aligned16(bias)) return fail(MNB_ERR_MISALIGNED, "%s: bias is not 16-byte aligned", fn);
-  const size_t need = mnb_workspace_bytes_f32(M, K, N, block_size);
+  // Required: the split activation and exponents, plus the small-M kernel's partials; the
+  // tensor-core kernel's partials (2M > 16) are optional.
+  size_t need = mnb_workspace_bytes_f32(M, K, N, block_size);
+  if (2 * M > 16) need -= mnb::gemm_tc_workspace_bytes(2 * M, K, N, block_size);
   if (ws_bytes < need)
     return fail(MNB_ERR_INVALID_ARG, "%s: workspace of %zu bytes, %zu needed", fn, ws_bytes, need);
   if (need > 0 && (st = check_ptr(fn, "workspace", workspace)) != MNB_OK) return st;
@@ -347,7 +356,8 @@ mnb_status mnb_gemm_f32(const float* A, int M, mnb_weight w, const uint8_t* repa
         e = mnb::launch_gemm_smallm_f32split(ctx, a2, M, q, K, N, block_size, Y, bias, rexp, a2 + head,
                                              ws_bytes - head);
       else
-        e = mnb::launch_gemm_tc_f32split(ctx, a2, M, q, repacked, K, N, block_size, Y, bias, rexp);
+        e = mnb::launch_gemm_tc_f32split(ctx, a2, M, q, repacked, K, N, block_size, Y, bias, rexp, a2 + head,
+                                         ws_bytes - head);
     }
   }
   if (e == cudaErrorNotSupported) e = mnb::launch_generic_f32(ctx, A, M, q, K, N, block_size, Y, bias);

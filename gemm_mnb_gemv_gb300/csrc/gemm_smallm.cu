@@ -716,6 +716,21 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
 
 }  // namespace
 
+cudaError_t launch_combine_slices(LaunchCtx& ctx, const float* part, int nslices, int M, int N, void* Y) {
+  const long long mn = (long long)M * N;
+  const long long blocks = (mn + 255) / 256, cap = (long long)ctx.num_sms * 8;
+  return launch_kernel(ctx, combine_slices_kernel, dim3((unsigned)(blocks < cap ? blocks : cap)), dim3(256), 0, part,
+                       nslices, mn, N, static_cast<__half*>(Y), static_cast<const __half*>(ctx.bias), ctx.bias_mode);
+}
+
+cudaError_t launch_combine_slices_f32(LaunchCtx& ctx, const float* part, int nslices, int Mout, int N, float* Yf,
+                                      const float* biasf, const int* rexp) {
+  const long long mn = (long long)Mout * N;
+  const long long blocks = (mn + 255) / 256, cap = (long long)ctx.num_sms * 8;
+  return launch_kernel(ctx, combine_slices_f32_kernel, dim3((unsigned)(blocks < cap ? blocks : cap)), dim3(256), 0,
+                       part, nslices, Mout, N, Yf, biasf, rexp);
+}
+
 cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
                                void* Y, void* workspace, size_t ws_bytes) {
   return launch_smallm_impl(ctx, A, M, w, K, N, bs, Y, M, nullptr, nullptr, nullptr, workspace, ws_bytes);

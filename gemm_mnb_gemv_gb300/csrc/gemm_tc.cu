@@ -68,7 +68,19 @@ struct TcArgs {
   float* Yf;
   const float* biasf;
   const int* rexp;
+  // Split-K (few output tiles): work item t is slice t % ksplit of tile t / ksplit, a range
+  // of whole quant groups (kunit k-blocks each); every item stores its fp32 partial
+  // part[slice][m][n] (rows of the activation operand), summed afterwards in slice order.
+  int ksplit, kunit;
+  float* part;
 };
+
+// k-block range [lo, hi) of slice `sl` (whole units of p.kunit k-blocks).
+__device__ __forceinline__ void slice_range(const TcArgs& p, int sl, int& lo, int& hi) {
+  const int nunits = p.kblocks / p.kunit;
+  lo = (sl * nunits / p.ksplit) * p.kunit;
+  hi = ((sl + 1) * nunits / p.ksplit) * p.kunit;
+}
 
 __device__ __forceinline__ uint32_t zp_byte(const TcArgs& p, int n, int byte_idx) {
   if (p.zp == nullptr || n >= p.N || byte_idx >= p.zrb) return 0x88u;
@@ -78,6 +90,7 @@ __device__ __forceinline__ uint32_t zp_byte(const TcArgs& p, int n, int byte_idx
 template <bool F32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const TcArgs p, const __grid_constant__ CUtensorMap tmap_a) {
+  const int ksplit = p.ksplit;  // K slices per tile (1: unsplit)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
   __shared__ uint64_t wready_bar[kWBufs];
@@ -89,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int KS = p.K / 16;                   // MMA k-steps per tile
-  const int ntile_total = p.mtiles * p.ntiles;
+  const int ntile_total = p.mtiles * p.ntiles * ksplit;  // work items
 
   if (tid == 0) {
     abort_flag = 0;
@@ -129,8 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
-        const int mt = t % p.mtiles, nt = t / p.mtiles;
-        for (int kb = 0; kb < p.kblocks; ++kb) {
+        const int tile = t / ksplit;
+        const int mt = tile % p.mtiles, nt = tile / p.mtiles;
+        int kb_lo, kb_hi;
+        slice_range(p, t % ksplit, kb_lo, kb_hi);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (issued >= kStages && !mbar_wait_bounded(&empty_bar[slot], phase ^ 1u)) {
             report_status(p.status, kStatusEmptyWait);
             atomicExch(&abort_flag, 1);
@@ -165,8 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ngroups = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
-        uint32_t ks = 0;
-        for (int kb = 0; kb < p.kblocks && ok; ++kb) {
+        int kb_lo, kb_hi;
+        slice_range(p, t % ksplit, kb_lo, kb_hi);
+        uint32_t ks = (uint32_t)kb_lo * 4u;  // absolute k-step (group boundaries)
+        for (int kb = kb_lo; kb < kb_hi && ok; ++kb) {
           // The dequantisers arrive on wready only after observing this stage's full
           // barrier (which also covers the activation box), so one wait orders both.
           if (!mbar_spin_bounded(&wready_bar[wb], wphase)) {
@@ -257,8 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const uint32_t w_u32 = smem_u32(smem) + kWOffset;
     for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
-      const int nt = t / p.mtiles;
+      const int nt = (t / ksplit) / p.mtiles;
       const int n = nt * kTileN + r;
+      int kb_lo, kb_hi;
+      slice_range(p, t % ksplit, kb_lo, kb_hi);
       // Zero-point byte(s) covering one 64-k stage: one byte for bs >= 32 (two groups at
       // most, sharing a byte), two bytes for bs = 16.
       auto zp_for = [&](int kb) -> uint32_t {
@@ -321,20 +341,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // Two zero-point registers, one per stage parity, each reloaded two stages ahead right
       // after its last use, so no register copy ever waits for a global load in flight.
-      uint32_t zeven = zp_for(0);
-      uint32_t zodd = p.kblocks > 1 ? zp_for(1) : 0u;
-      for (int kb = 0; kb < p.kblocks && ok; kb += 2) {
+      uint32_t zeven = zp_for(kb_lo);
+      uint32_t zodd = kb_lo + 1 < kb_hi ? zp_for(kb_lo + 1) : 0u;
+      for (int kb = kb_lo; kb < kb_hi && ok; kb += 2) {
         if (!do_stage(kb, zeven)) {
           ok = false;
           break;
         }
-        if (kb + 2 < p.kblocks) zeven = zp_for(kb + 2);
-        if (kb + 1 < p.kblocks) {
+        if (kb + 2 < kb_hi) zeven = zp_for(kb + 2);
+        if (kb + 1 < kb_hi) {
           if (!do_stage(kb + 1, zodd)) {
             ok = false;
             break;
           }
-          if (kb + 3 < p.kblocks) zodd = zp_for(kb + 3);
+          if (kb + 3 < kb_hi) zodd = zp_for(kb + 3);
         }
       }
       if (!ok) {
@@ -352,9 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long gc = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntile_total && ok; t += gridDim.x) {
-      const int mt = t % p.mtiles, nt = t / p.mtiles;
+      const int tile = t / ksplit, sl = t % ksplit;
+      const int mt = tile % p.mtiles, nt = tile / p.mtiles;
       const int n = nt * kTileN + quarter * 32 + lane;
       const bool nval = n < p.N;
+      int kb_lo, kb_hi;
+      slice_range(p, sl, kb_lo, kb_hi);
+      const int g_lo = (kb_lo * kStageK) / p.bs;
+      const int g_hi = ksplit > 1 ? (kb_hi * kStageK) / p.bs : p.G;
       float acc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
@@ -364,10 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         return p.scales_f16 ? half_bits_to_float(ld_nc_u16(p.scales + 2 * si))
                             : __uint_as_float(ld_nc_u32(p.scales + 4 * si));
       };
-      float s_next = scale_of(0);
-      for (int g = 0; g < p.G; ++g) {
+      float s_next = scale_of(g_lo);
+      for (int g = g_lo; g < g_hi; ++g) {
         const float s = s_next;
-        if (g + 1 < p.G) s_next = scale_of(g + 1);
+        if (g + 1 < g_hi) s_next = scale_of(g + 1);
         const uint32_t b = (uint32_t)(gc & 1);
         if (!mbar_wait_bounded(&tfull_bar[b], (uint32_t)((gc >> 1) & 1))) {
           report_status(p.status, kStatusMmaWait);
@@ -391,7 +416,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gc;
       }
       if (!ok) break;
-      if (nval) {
+      if (ksplit > 1) {
+       if (nval) {
+        // plain fp32 partial of this slice, every row of the activation operand
+        float* pc = p.part + (long long)sl * p.M * p.N + n;
+        const int m0 = mt * kTileM + half * 128;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          const int m = m0 + i;
+          if (m < p.M) pc[(long long)m * p.N] = acc[i];
+        }
+       }
+      } else if (nval) {
         const int m0 = mt * kTileM + half * 128;
         if constexpr (F32) {
           const float b = p.biasf ? p.biasf[n] : 0.0f;
@@ -415,12 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (abort_flag) {
       // A wait gave up somewhere: mark this CTA's outputs as invalid.
       for (int t = blockIdx.x; t < ntile_total; t += gridDim.x) {
-        const int mt = t % p.mtiles, nt = t / p.mtiles;
+        const int tile = t / ksplit;
+        const int mt = tile % p.mtiles, nt = tile / p.mtiles;
         const int n = nt * kTileN + quarter * 32 + lane;
         if (n >= p.N) continue;
         for (int i = 0; i < 128; ++i) {
           const int m = mt * kTileM + half * 128 + i;
-          if constexpr (F32) {
+          if (ksplit > 1) {
+            if (m < p.M) p.part[((long long)(t % ksplit) * p.M + m) * p.N + n] = __uint_as_float(0x7fc00000u);
+          } else if constexpr (F32) {
             if ((m & 1) == 0 && (m >> 1) < p.Mout) p.Yf[(long long)(m >> 1) * p.N + n] = __uint_as_float(0x7fc00000u);
           } else {
             if (m < p.M) p.Y[(long long)m * p.N + n] = __ushort_as_half(0x7e00);
@@ -460,8 +499,26 @@ void* tensor_map_encode_fn() { return reinterpret_cast<void*>(get_encode()); }
 
 namespace {
 
+// K slices for an M-row (activation operand) x N output on num_sms SMs: 1 unless the
+// output has fewer tiles than half the SMs; slices are whole quant groups of at least four
+// 64-k blocks, at most 32 of them.
+int tc_ksplit(int M, int K, int N, int bs, int num_sms) {
+  if (K % kStageK != 0 || K % bs != 0) return 1;
+  const int tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
+  if (2 * tiles > num_sms) return 1;
+  const int kblocks = K / kStageK, unit = bs > kStageK ? bs / kStageK : 1;
+  int ks = num_sms / tiles;
+  if (ks > kblocks / 4) ks = kblocks / 4;
+  if (ks > kblocks / unit) ks = kblocks / unit;
+  if (ks > 32) ks = 32;
+  return ks < 2 ? 1 : ks;
+}
+
+constexpr int kMaxSms = 160;  // workspace sizing covers any GPU with up to this many SMs
+
 cudaError_t launch_tc_impl(LaunchCtx& ctx, const void* A, int M, const QWeight& w, const uint8_t* repacked, int K,
-                           int N, int bs, void* Y, int Mout, float* Yf, const float* biasf, const int* rexp) {
+                           int N, int bs, void* Y, int Mout, float* Yf, const float* biasf, const int* rexp,
+                           void* workspace, size_t ws_bytes) {
   if (K % 16 != 0) return cudaErrorNotSupported;
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
@@ -496,27 +553,40 @@ cudaError_t launch_tc_impl(LaunchCtx& ctx, const void* A, int M, const QWeight& 
   a.Yf = Yf;
   a.biasf = biasf;
   a.rexp = rexp;
-  const int tiles = a.mtiles * a.ntiles;
-  const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+  a.ksplit = tc_ksplit(M, K, N, bs, ctx.num_sms);
+  if (a.ksplit > 1 && (workspace == nullptr || ws_bytes < (size_t)a.ksplit * M * N * 4)) a.ksplit = 1;
+  a.kunit = bs > kStageK ? bs / kStageK : 1;
+  a.part = static_cast<float*>(workspace);
+  const int items = a.mtiles * a.ntiles * a.ksplit;
+  const int grid = items < ctx.num_sms ? items : ctx.num_sms;
   const bool f32 = Yf != nullptr;
   auto kern = f32 ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  e = launch_kernel(ctx, kern, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, a, tmap);
   ctx.variant = f32 ? "gemm_tcgen05_w128xa256_f32split" : "gemm_tcgen05_w128xa256";
-  return launch_kernel(ctx, kern, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, a, tmap);
+  if (e != cudaSuccess || a.ksplit == 1) return e;
+  ctx.variant = f32 ? "gemm_tcgen05_w128xa256_f32split_splitk" : "gemm_tcgen05_w128xa256_splitk";
+  if (f32) return launch_combine_slices_f32(ctx, a.part, a.ksplit, Mout, N, Yf, biasf, rexp);
+  return launch_combine_slices(ctx, a.part, a.ksplit, M, N, Y);
 }
 
 }  // namespace
 
+size_t gemm_tc_workspace_bytes(int M_rows, int K, int N, int bs) {
+  const int ks = tc_ksplit(M_rows, K, N, bs, kMaxSms);
+  return ks > 1 ? (size_t)ks * M_rows * N * 4 : 0;
+}
+
 cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& w,
-                           const uint8_t* repacked, int K, int N, int bs, void* Y) {
-  return launch_tc_impl(ctx, A, M, w, repacked, K, N, bs, Y, M, nullptr, nullptr, nullptr);
+                           const uint8_t* repacked, int K, int N, int bs, void* Y, void* workspace, size_t ws_bytes) {
+  return launch_tc_impl(ctx, A, M, w, repacked, K, N, bs, Y, M, nullptr, nullptr, nullptr, workspace, ws_bytes);
 }
 
 cudaError_t launch_gemm_tc_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w,
                                     const uint8_t* repacked, int K, int N, int bs, float* Y, const float* bias,
-                                    const int* rexp) {
-  return launch_tc_impl(ctx, A2, 2 * M, w, repacked, K, N, bs, nullptr, M, Y, bias, rexp);
+                                    const int* rexp, void* workspace, size_t ws_bytes) {
+  return launch_tc_impl(ctx, A2, 2 * M, w, repacked, K, N, bs, nullptr, M, Y, bias, rexp, workspace, ws_bytes);
 }
 
 }  // namespace mnb

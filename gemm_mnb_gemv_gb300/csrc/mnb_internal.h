@@ -59,9 +59,14 @@ cudaError_t launch_gemm_smallm(LaunchCtx& ctx, const void* A, int M, const QWeig
                                void* Y, void* workspace, size_t ws_bytes);
 int smallm_kslice(int M, int K, int bs, int ssz, bool zp);
 size_t smallm_workspace_bytes(int M, int K, int N, int bs);
-// M > 16 on the tcgen05 tensor cores, reading the repacked operand.
+// M > 16 on the tcgen05 tensor cores, reading the repacked operand.  With a workspace of
+// at least gemm_tc_workspace_bytes (the sizing for up to 160 SMs), shapes with fewer
+// output tiles than half the SMs split K into slices of whole quant groups and sum their
+// fp32 partials in slice order; without one they run unsplit.
 cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& w,
-                           const uint8_t* repacked, int K, int N, int bs, void* Y);
+                           const uint8_t* repacked, int K, int N, int bs, void* Y, void* workspace = nullptr,
+                           size_t ws_bytes = 0);
+size_t gemm_tc_workspace_bytes(int M_rows, int K, int N, int bs);
 // fp32 activations.  M = 1: bulk-copy GEMV with fp32 activations (K <= 16384).  M >= 2:
 // rows split into fp16 hi/lo pairs (A2 holds 2M rows, rexp M exponents), then the small-M
 // kernel (2M <= 16) or the tcgen05 kernel with the pair-summing fp32 epilogue.  The generic
@@ -69,12 +74,17 @@ cudaError_t launch_gemm_tc(LaunchCtx& ctx, const void* A, int M, const QWeight& 
 cudaError_t launch_gemv_f32_tma(LaunchCtx& ctx, const float* A, const QWeight& w, int K, int N, int bs,
                                 float* Y, const float* bias);
 cudaError_t launch_split_f32(LaunchCtx& ctx, const float* A, int M, int K, void* A2, int* rexp);
+// Fixed-order sums of K-slice partials part[slice][rows][N]: fp16 Y with ctx's bias mode,
+// or fp32 Yf from hi/lo row pairs with their exponents (split fp32 activations).
+cudaError_t launch_combine_slices(LaunchCtx& ctx, const float* part, int nslices, int M, int N, void* Y);
+cudaError_t launch_combine_slices_f32(LaunchCtx& ctx, const float* part, int nslices, int Mout, int N, float* Yf,
+                                      const float* biasf, const int* rexp);
 cudaError_t launch_gemm_smallm_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w, int K, int N,
                                         int bs, float* Y, const float* bias, const int* rexp,
                                         void* workspace = nullptr, size_t ws_bytes = 0);
 cudaError_t launch_gemm_tc_f32split(LaunchCtx& ctx, const void* A2, int M, const QWeight& w,
                                     const uint8_t* repacked, int K, int N, int bs, float* Y, const float* bias,
-                                    const int* rexp);
+                                    const int* rexp, void* workspace = nullptr, size_t ws_bytes = 0);
 cudaError_t launch_generic_f32(LaunchCtx& ctx, const float* A, int M, const QWeight& w, int K, int N, int bs,
                                float* Y, const float* bias);
 // Any M, any K % 16 == 0: CUDA-core kernel, fp32 arithmetic.

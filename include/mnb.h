@@ -118,13 +118,17 @@ MNB_API mnb_status mnb_gemv(const void *A, mnb_weight w, int K, int N, int block
                     mnb_stream stream);
 
 /*
- * Scratch bytes mnb_gemm (and mnb_gemm_bias) needs for this shape (0 when none). Only
- * 2 <= M <= 16 with K too large for one shared-memory pass of the small-M kernel needs
- * any: K is then split into slices whose fp32 partials ([slices, M, N]) are summed in
- * slice order, so results stay deterministic. The size is an upper bound over the scale
- * dtype and zero points (the call may use less). The caller allocates it once and passes it
- * to every call of that shape; its contents need no initialisation, each call overwrites
- * them, so calls sharing one workspace must be ordered on one stream.
+ * Scratch bytes for mnb_gemm (and mnb_gemm_bias) at this shape (0 when none): fp32
+ * partials ([slices, M, N]) of a K split, summed in slice order, so results stay
+ * deterministic.
+ *   2 <= M <= 16: required when K is too large for one shared-memory pass of the small-M
+ *   kernel; the size is an upper bound over the scale dtype and zero points.
+ *   M > 16: optional; with it, outputs with fewer 128 x 256 tiles than half the SMs split
+ *   K (whole quant groups) over the SMs, without it they run unsplit. The size covers
+ *   GPUs of up to 160 SMs.
+ * The caller allocates it once and passes it to every call of that shape; its contents
+ * need no initialisation, each call overwrites them, so calls sharing one workspace must
+ * be ordered on one stream.
  */
 MNB_API size_t mnb_workspace_bytes(int M, int K, int N, int block_size);
 
@@ -136,7 +140,7 @@ MNB_API size_t mnb_workspace_bytes(int M, int K, int N, int block_size);
  * tcgen05 tensor cores,
  * the group scale applied to each group's partial accumulator (marlin_gemm.rs,
  * matmul_nbits_marlin_gemm_f16). `workspace`/`ws_bytes`: see mnb_workspace_bytes;
- * a smaller workspace gives MNB_ERR_INVALID_ARG.
+ * for 2 <= M <= 16 a smaller workspace gives MNB_ERR_INVALID_ARG.
  */
 MNB_API mnb_status mnb_gemm(const void *A, int M, mnb_weight w, const uint8_t *repacked, int K, int N,
                     int block_size, void *workspace, size_t ws_bytes, void *Y,
@@ -187,10 +191,10 @@ MNB_API mnb_status mnb_gemv_gate_up_swiglu(const void *A, mnb_weight gate, mnb_w
  */
 
 /*
- * Workspace bytes mnb_gemm_f32 needs: 0 for M = 1, else 4*M*K (the split activation) +
- * 4*M rounded up to 16 (row exponents), plus for 2 <= M <= 8 with K beyond one
- * shared-memory pass the fp32 K-slice partials of the 2*M split rows
- * (mnb_workspace_bytes(2*M, K, N, block_size) bytes).
+ * Workspace bytes for mnb_gemm_f32: 0 for M = 1, else 4*M*K (the split activation) +
+ * 4*M rounded up to 16 (row exponents) + mnb_workspace_bytes(2*M, K, N, block_size)
+ * (the K-slice partials of the 2*M split rows: required for M <= 8, optional above, as
+ * in mnb_gemm).
  */
 MNB_API size_t mnb_workspace_bytes_f32(int M, int K, int N, int block_size);
 

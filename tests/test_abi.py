@@ -70,12 +70,16 @@ def test_workspace_bytes_f32_layout(lib):
     for M, K, N, bs in [(2, 4096, 4096, 64), (4, 14336, 256, 32), (8, 12288, 96, 128), (9, 4096, 512, 32),
                         (300, 1024, 200, 32)]:
         head = 4 * M * K + (4 * M + 15) // 16 * 16
-        part = mnb.mnb_workspace_bytes(2 * M, K, N, bs) if 2 * M <= 16 else 0
-        assert mnb.mnb_workspace_bytes_f32(M, K, N, bs) == head + part
+        assert mnb.mnb_workspace_bytes_f32(M, K, N, bs) == head + mnb.mnb_workspace_bytes(2 * M, K, N, bs)
     # one shared-memory pass: no partials; K well beyond it: partials of every slice
     assert mnb.mnb_workspace_bytes(8, 4096, 4096, 64) == 0
     assert mnb.mnb_workspace_bytes(8, 14336, 256, 32) % (8 * 256 * 4) == 0
     assert mnb.mnb_workspace_bytes(8, 14336, 256, 32) >= 2 * 8 * 256 * 4
+    # M > 16: partials for a K split over the SMs when the output has few tiles, none when
+    # it has enough tiles for every SM
+    assert mnb.mnb_workspace_bytes(17, 4096, 4096, 64) == 5 * 17 * 4096 * 4
+    assert mnb.mnb_workspace_bytes(2048, 4096, 14336, 128) == 0
+    assert mnb.mnb_workspace_bytes(300, 1000, 200, 8) == 0  # invalid block size: no split
 
 
 def _w(packed=16, scales=16, dtype=0, zp=None):

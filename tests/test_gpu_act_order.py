@@ -151,7 +151,7 @@ def test_gemm_act_order_parity(env, name, M, K, N, bs, sdt, zp, kind):
     if name == "ao_gemv_bigk":
         assert variant == "gemv_tma_ring", variant  # separate gather, then the GEMV
     if M > 16:
-        assert variant == tc_variant(N), variant
+        assert variant.startswith(tc_variant(N)), variant
     if name.startswith("ao_small_bigk"):
         assert variant == "gemm_smallm_mma16816_splitk", variant
     mnb.mnb_check_device_status()

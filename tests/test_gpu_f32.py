@@ -57,6 +57,7 @@ F32_CASES = [
     ("f32_m4_k14336", 4, 14336, 256, 32, "f32", False, "normal", True, "gemm_smallm_mma16816_f32split_splitk"),
     ("f32_m2_k12288_wide", 2, 12288, 144, 128, "f16", True, "wide", False, "gemm_smallm_mma16816_f32split_splitk"),
     ("f32_m7_k8192", 7, 8192, 96, 64, "f32", True, "normal", True, "gemm_smallm_mma16816_f32split_splitk"),
+    ("f32_m12_tc_splitk", 12, 2048, 256, 64, "f16", True, "wide", True, "gemm_tcgen05_w128xa256_f32split_splitk"),
 ]
 
 
@@ -73,7 +74,8 @@ def test_gemm_f32_parity(env, name, M, K, N, bs, sdt, zp, recipe, has_bias, vari
         Y = Y + bias.astype(np.float64)[None, :]
         B = B + 2.0 ** -24 / 2e-3 * np.abs(bias.astype(np.float64))[None, :]
     assert_within_bound(y, Y, B, name)
-    assert got_variant == variant
+    # the tensor-core kernel splits K over the SMs when the output has few tiles
+    assert got_variant == variant or (variant.startswith("gemm_tcgen05") and got_variant == variant + "_splitk")
     mnb.mnb_check_device_status()
 
 

@@ -219,7 +219,7 @@ def test_gemm_large_m_ragged(env, M, K, N, bs, sdt, zp):
     packed, scales, zpt = upload_weight(w, dev)
     rp = mnb.mnb_repack(packed, K, N, bs)
     y = mnb.mnb_gemm(upload_act(A, dev), packed, scales, zpt, K, N, bs, repacked=rp)
-    assert mnb.mnb_last_variant() == tc_variant(N)
+    assert mnb.mnb_last_variant().startswith(tc_variant(N))
     torch.cuda.synchronize()
     mnb.mnb_check_device_status()
     Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
@@ -325,6 +325,33 @@ def test_graph_capture_replay_matches_eager(env):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(y1, e1) and torch.equal(y4, e4)
+
+
+# M > 16 with few output tiles: K split over the SMs (fp32 partials, summed in slice order).
+@pytest.mark.parametrize("M,K,N,bs,sdt,zp", [(17, 4096, 512, 64, "f16", True), (40, 2048, 256, 128, "f32", False),
+                                             (256, 4096, 384, 32, "f16", True), (100, 1024, 130, 16, "f16", True)])
+def test_gemm_tc_split_k(env, M, K, N, bs, sdt, zp):
+    mnb, torch, dev = env
+    wl = syn.custom(f"tcsk_{M}_{K}_{N}_{bs}", M, K, N, bs, scales_dtype=sdt, has_zp=zp)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    packed, scales, zpt = upload_weight(w, dev)
+    rp = mnb.mnb_repack(packed, K, N, bs)
+    a = upload_act(A, dev)
+    y = mnb.mnb_gemm(a, packed, scales, zpt, K, N, bs, repacked=rp)
+    torch.cuda.synchronize()
+    assert mnb.mnb_last_variant() == "gemm_tcgen05_w128xa256_splitk"
+    y2 = mnb.mnb_gemm(a, packed, scales, zpt, K, N, bs, repacked=rp)
+    # without a workspace the same call runs unsplit
+    y0 = mnb.mnb_gemm(a, packed, scales, zpt, K, N, bs, repacked=rp,
+                      workspace=torch.empty(0, dtype=torch.uint8, device=dev))
+    torch.cuda.synchronize()
+    assert mnb.mnb_last_variant() == "gemm_tcgen05_w128xa256"
+    mnb.mnb_check_device_status()
+    assert torch.equal(y, y2)  # deterministic
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
+    assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
+    assert_within_bound(y0.cpu().numpy(), Y, B, wl.name + " unsplit")
 
 
 def test_small_m_pairs_graph_and_programmatic_launch(env):
