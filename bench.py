@@ -594,6 +594,9 @@ def main():
         extras["f32_attn"] = db.gemm_f32(wl, 20, 3, sampler, calls=200)
         extras["f32_prefill"] = db.gemm_f32(syn.WORKLOADS["prefill_m2048_k4096_n14336"], 5, 3, sampler, calls=5)
     for k, v in extras.items():
+        if "us_per_call" not in v:  # derived entries (ratios)
+            log(f"{k}: {json.dumps(v)}")
+            continue
         log(f"{k}: {v['us_per_call']:.3f} us/call, {v.get('gbps', 0):.1f} GB/s, "
             f"{v.get('tflops', 0):.1f} TFLOP/s ({v['variant']})")
     clocks = sampler.stop()
