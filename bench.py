@@ -582,6 +582,9 @@ def main():
         # the pages' concern is a cliff from M = 1 to M = 2
         extras["verify_over_m1"] = {f"M{M}": extras[f"verify_m{M}"]["us_per_call"] / head["us_per_call"]
                                     for M in (2, 4, 8, 16)}
+        # mid-size M on the tensor-core kernel (verify storage): few output tiles, K split
+        extras["mid_m64"] = db.gemm(syn.custom("mid_m64_k4096_n4096", 64, 4096, 4096, 64), 20, 3, sampler,
+                                    calls=100, repacked=True, shared_act=True)
         extras["prefill"] = db.gemm(syn.WORKLOADS["prefill_m2048_k4096_n14336"], 10, 3, sampler,
                                     calls=9, repacked=True)
         extras["mlp_chain"] = db.mlp_chain(10, 3, sampler)
