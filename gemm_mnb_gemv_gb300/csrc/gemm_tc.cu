@@ -56,6 +56,8 @@ struct TcArgs {
   __half* Y;
   int M, N, K, bs, G, zrb;
   int kblocks;  // ceil(K / 64)
+  int nmma;     // MMA N = activation rows per tile: 256, or M rounded up to 16 when M < 256
+                // (one tile row; accumulator columns past it are never written nor stored)
   int mtiles, ntiles;
   uint32_t* status;
   const __half* bias;
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[slot], kXBytes + kPBytes);
+          mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(p.nmma * kStageK * 2 + kPBytes));
           tc::tma_load_2d(stage_x(slot), &tmap_a, kb * kStageK, mt * kTileM, &full_bar[slot]);
           bulk_g2s(stage_p(slot), p.repacked + ((long long)nt * p.kblocks + kb) * kPBytes, kPBytes,
                    &full_bar[slot]);
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // it: the four descriptors of a stage are formed before its first MMA, group
       // boundaries are precomputed, and waits spin without suspending.
       pdl_launch_dependents();
-      const uint32_t idesc = tc::idesc_f16_f32(kTileN, kTileM);
+      const uint32_t idesc = tc::idesc_f16_f32(kTileN, p.nmma);
       const uint64_t dx0 = tc::smem_desc_k_sw128(smem_u32(smem));
       const uint64_t dw0 = tc::smem_desc_k_sw128(smem_u32(smem) + kWOffset);
       const uint32_t kpg_mask = (uint32_t)(p.bs / 16) - 1u;  // k-steps per group - 1
@@ -525,7 +527,8 @@ cudaError_t launch_tc_impl(LaunchCtx& ctx, const void* A, int M, const QWeight& 
   CUtensorMap tmap;
   const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
   const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kStageK, (cuuint32_t)kTileM};
+  const int nmma = M >= kTileM ? kTileM : (M + 15) / 16 * 16;
+  const cuuint32_t box[2] = {(cuuint32_t)kStageK, (cuuint32_t)nmma};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(A), gdim, gstride, box,
                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -544,6 +547,7 @@ cudaError_t launch_tc_impl(LaunchCtx& ctx, const void* A, int M, const QWeight& 
   a.G = K / bs;
   a.zrb = (a.G + 1) / 2;
   a.kblocks = (K + kStageK - 1) / kStageK;
+  a.nmma = nmma;
   a.mtiles = (M + kTileM - 1) / kTileM;
   a.ntiles = (N + kTileN - 1) / kTileN;
   a.status = ctx.status;
