@@ -400,12 +400,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
 // the conversion and FMA pipes issuing while the ring streams.
 constexpr int kNCW = 16;
 constexpr int kRingBudget = 180 * 1024;
+// The paired kernel's stages hold twice the bytes; three of them need a larger ring (a
+// larger ring did not help the single-weight kernel).
+constexpr int kRingBudgetPair = 210 * 1024;
 
 using TmaKernel = void (*)(const TmaGemvArgs);
 
 template <int WG, int CPS, bool PAIR>
 TmaKernel pick(bool bs16, bool s16, bool zp) {
-  constexpr int VPG = PAIR ? 2 : 4;
+  // Columns per lane group and stage: four; two for the pair beyond one chunk per lane,
+  // whose stages would not fit the ring otherwise.
+  constexpr int VPG = (PAIR && CPS > 1) ? 2 : 4;
 #define MNB_PICK(B, S, Z) gemv_tma_kernel<kNCW, WG, CPS, VPG, B, PAIR, S, Z>
   if (bs16) {
     if (s16) return zp ? MNB_PICK(true, true, true) : MNB_PICK(true, true, false);
@@ -495,7 +500,7 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   }
   if (ga && cps != 1) return cudaErrorNotSupported;
   const int ng = kNCW / wg;
-  const int cb = ng * (PAIR ? 2 : 4);
+  const int cb = ng * ((PAIR && cps > 1) ? 2 : 4);
   const int G = K / bs;
   const bool s16 = w[0].scales_f16 != 0;
   const bool zp = w[0].zp != nullptr;
@@ -528,7 +533,7 @@ cudaError_t launch_tma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   a.stage_bytes = cb * NWT * (a.row_bytes + a.sbytes + a.zbytes);
   // Shared copies of A and of the permuted A' for the gather.
   const int abytes = ga ? (Ka * 2 + 15) / 16 * 16 + K * 2 : 0;
-  const int ring_budget = kRingBudget - abytes;
+  const int ring_budget = (PAIR ? kRingBudgetPair : kRingBudget) - abytes;
   if (a.stage_bytes * 2 > ring_budget) return cudaErrorNotSupported;
   a.stages = ring_budget / a.stage_bytes;
   if (a.stages > kMaxStages) a.stages = kMaxStages;
