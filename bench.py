@@ -508,6 +508,32 @@ def run_single(db, name, steps, warmup):
 
 
 # ---------------------------------------------------------------------------------
+def secondary_lines(extras: dict) -> list:
+    """One log line per secondary entry: timings, or the JSON of derived entries (ratios)."""
+    out = []
+    for k, v in extras.items():
+        if "us_per_call" not in v:
+            out.append(f"{k}: {json.dumps(v)}")
+            continue
+        out.append(f"{k}: {v['us_per_call']:.3f} us/call, {v.get('gbps', 0):.1f} GB/s, "
+                   f"{v.get('tflops', 0):.1f} TFLOP/s ({v.get('variant', '?')})")
+    return out
+
+
+def annotate_secondary(extras: dict, hbm: float, tc: float, peak_src: str) -> dict:
+    """Roofline of the prefill entry against the tensor peak, HBM fraction of the others
+    (not of the labelled hot-L2 entry)."""
+    pf = extras.get("prefill")
+    if pf is not None:
+        pf["roofline"] = {"bound": "tensor", "achieved": pf["tflops"], "peak": tc, "unit": "TFLOP/s",
+                          "frac": pf["tflops"] / tc,
+                          "peak_source": f"{peak_src} bf16_tflops (burst; fp16 rate equals bf16)"}
+    for k, v in extras.items():
+        if "gbps" in v and k not in ("prefill", "headline_hot_l2"):
+            v["hbm_frac"] = v["gbps"] / hbm
+    return extras
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -596,12 +622,8 @@ def main():
         extras["act_order_attn"] = db.act_order(wl, 20, 3, sampler)
         extras["f32_attn"] = db.gemm_f32(wl, 20, 3, sampler, calls=200)
         extras["f32_prefill"] = db.gemm_f32(syn.WORKLOADS["prefill_m2048_k4096_n14336"], 5, 3, sampler, calls=5)
-    for k, v in extras.items():
-        if "us_per_call" not in v:  # derived entries (ratios)
-            log(f"{k}: {json.dumps(v)}")
-            continue
-        log(f"{k}: {v['us_per_call']:.3f} us/call, {v.get('gbps', 0):.1f} GB/s, "
-            f"{v.get('tflops', 0):.1f} TFLOP/s ({v['variant']})")
+    for msg in secondary_lines(extras):
+        log(msg)
     clocks = sampler.stop()
     e2e = db.e2e_gemv(head, max(3, args.steps // 10))
 
@@ -628,14 +650,7 @@ def main():
             "gpu_launches": launches_headline}
     if extras:
         tc = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        pf = extras["prefill"]
-        pf["roofline"] = {"bound": "tensor", "achieved": pf["tflops"], "peak": tc, "unit": "TFLOP/s",
-                          "frac": pf["tflops"] / tc,
-                          "peak_source": f"{peak_src} bf16_tflops (burst; fp16 rate equals bf16)"}
-        for k, v in extras.items():
-            if "gbps" in v and k not in ("prefill", "headline_hot_l2"):
-                v["hbm_frac"] = v["gbps"] / hbm
-        line["secondary"] = extras
+        line["secondary"] = annotate_secondary(extras, hbm, tc, peak_src)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(4.0 if args.quick else 12.0)
     if rank == 0:
