@@ -93,28 +93,6 @@ __device__ __forceinline__ void group_bar(int gi) {
   asm volatile("bar.sync %0, %1;" ::"r"(2 + gi), "n"(kGW * 32) : "memory");
 }
 
-// Every thread of both CTAs of the pair; also orders the mbarrier inits before any
-// multicast copy that signals them.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// 1-D bulk copy into the same shared-memory offset of every CTA in `mask`, each of which
-// sees `bytes` complete on its own mbarrier at `bar`'s offset.
-__device__ __forceinline__ void bulk_g2s_multicast(void* dst_smem, const void* src_gmem, uint32_t bytes,
-                                                   uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;"
-      ::"r"(smem_u32(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
 // Fixed-order sum over the K slices of the staged partials of activation row m, weight row
 // `row` of the tile.
 template <int MSETS>
@@ -130,15 +108,13 @@ __device__ __forceinline__ float slice_sum(const float (&red)[kGW][MSETS][32][4]
 // CPG: 32-k chunks per quant group (block size 32, 64 or 128).  The scale dtype is a
 // runtime property (one uniform branch per group); zero points are a template flag.
 //
-// Two row sets (M > 8) run as CTA pairs: each CTA of the pair bulk-copies every other
-// activation row into both CTAs' shared memory (row stride 64 mod 128 bytes, so the two
-// rows a quarter-warp reads sit in different banks), halving the activation reads from
-// L2; lanes pair the halves after loading them.  One row set stages the fragment order,
-// with plain loads.
+// Two row sets (M > 8) stage the activation rows by one bulk copy per row (row stride 64
+// mod 128 bytes, so the two rows a quarter-warp reads sit in different banks); lanes pair
+// the halves after loading them.  One row set stages the fragment order, with plain loads.
 template <int MSETS, int CPG, bool ZP, bool F32 = false, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_smallm_kernel(const SmArgs p, const __grid_constant__ CUtensorMap tmap_s) {
-  constexpr bool kPair = MSETS == 2;
+  constexpr bool kTwoSets = MSETS == 2;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ uint64_t x_bar;
@@ -152,13 +128,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int C = klen >> 5;                         // 32-k chunks in the slice
   const int gb = SPLIT ? (k0 >> p.gshift) : 0;     // first group of the slice
   const int S = p.stages;
-  // shared memory: [ring stages][activations: fragment order (one row set) or rows (pairs)]
+  // shared memory: [ring stages][activations: fragment order (one row set) or rows (two sets)]
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned slots
   uint8_t* xs = ring + (size_t)S * p.stage_bytes;
   const int t_begin = blockIdx.x * p.tiles_per_cta;
   const int t_end = min(p.ntiles, t_begin + p.tiles_per_cta);
-  const int ntile = max(0, t_end - t_begin);  // a pair's padding CTA has none
+  const int ntile = max(0, t_end - t_begin);
 
   if (tid == 0) {
     failed = 0;
@@ -166,11 +142,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kGW);
     }
-    if (kPair) mbar_init(&x_bar, 1);
+    if (kTwoSets) mbar_init(&x_bar, 1);
     fence_mbar_init();
   }
-  if constexpr (kPair) cluster_sync_all();
-  else __syncthreads();
+  __syncthreads();
   bool x_issued = false, x_ok = true;
 
   if (warp == kCW) {
@@ -224,14 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
     pdl_wait();
     const uint32_t xs_u32 = smem_u32(xs);
-    if constexpr (kPair) {
-      // This CTA's activation rows (every other one) go to both CTAs of the pair.
+    if constexpr (kTwoSets) {
+      // One lane copies every activation row of the slice into this CTA's shared memory.
       if (warp == 0 && lane == 0) {
-        const int rank = (int)cluster_rank();
         mbar_arrive_expect_tx(&x_bar, (uint32_t)(p.M * klen * 2));
-        for (int m = rank; m < p.M; m += 2)
-          bulk_g2s_multicast(xs + (size_t)m * p.xstride, p.A + (long long)m * p.K + k0, (uint32_t)(klen * 2),
-                             &x_bar, (uint16_t)0x3);
+        for (int m = 0; m < p.M; ++m)
+          bulk_g2s(xs + (size_t)m * p.xstride, p.A + (long long)m * p.K + k0, (uint32_t)(klen * 2), &x_bar);
         x_issued = true;
       }
       if (!mbar_wait_bounded(&x_bar, 0)) {
@@ -281,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t xlane = xs_u32 + (uint32_t)lane * 16u;
     const uint32_t xcstride = 64u * (uint32_t)p.M;
     bool xlive[MSETS];
-    uint32_t xrow[MSETS];  // pair layout: this lane's 16 bytes of row 8s + g, chunk 0
+    uint32_t xrow[MSETS];  // two-set layout: this lane's 16 bytes of row 8s + g, chunk 0
 #pragma unroll
     for (int s = 0; s < MSETS; ++s) {
       xlive[s] = 8 * s + g < p.M;
@@ -359,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < MSETS; ++s) {
             uint4 xf = make_uint4(0, 0, 0, 0);
             if (xlive[s]) {
-              if constexpr (kPair) {
+              if constexpr (kTwoSets) {
                 uint32_t q[4];
                 pair_halves_stride4(lds128_a(xrow[s] + 64u * (uint32_t)c), q);
                 xf = make_uint4(q[0], q[1], q[2], q[3]);
@@ -420,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < MSETS; ++s) {
               uint4 xf = make_uint4(0, 0, 0, 0);
               if (xlive[s]) {
-                if constexpr (kPair) {
+                if constexpr (kTwoSets) {
                   uint32_t q[4];
                   pair_halves_stride4(lds128_a(xrow[s] + 64u * c), q);
                   xf = make_uint4(q[0], q[1], q[2], q[3]);
@@ -487,11 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       group_bar(gi);
     }
   }
-  if constexpr (kPair) {
-    // Neither CTA of the pair leaves while a copy it issued may still land in the other.
+  if constexpr (kTwoSets) {
+    // The CTA does not leave while an activation copy it issued may still land.
     if (x_issued && !x_ok) (void)mbar_wait_bounded(&x_bar, 0);
-    __syncwarp();
-    cluster_sync_all();
   }
 }
 
@@ -551,14 +522,14 @@ SmKernel pick(int cpg, bool zp) {
 // mod 32 bytes, so row r starts at bank 4 * (r * odd mod 8) and eight rows never collide.
 static int scale_stride(int bytes) { return bytes % 32 == 0 ? bytes + 16 : bytes; }
 
-// Activation row stride of the CTA-pair layout for a slice of ks k (2 * ks is a multiple of
+// Activation row stride of the two-row-set layout for a slice of ks k (2 * ks is a multiple of
 // 64): congruent to 64 mod 128 bytes.
-static int pair_x_stride(int ks) { return (2 * ks) % 128 == 0 ? 2 * ks + 64 : 2 * ks; }
+static int two_set_x_stride(int ks) { return (2 * ks) % 128 == 0 ? 2 * ks + 64 : 2 * ks; }
 
 // Shared memory for the staged activations of a slice of ks k.
 static size_t x_bytes(int M, int ks) {
   if (M <= 8) return (size_t)2 * M * ks;  // one row set, compact fragment order
-  return (size_t)M * pair_x_stride(ks);
+  return (size_t)M * two_set_x_stride(ks);
 }
 
 // K-slice length for the small-M kernel: all of K when its rows, scales and activations fit
@@ -662,7 +633,7 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   }
   const int msets = M <= 8 ? 1 : 2;
   const size_t xbytes = x_bytes(M, ks);
-  a.xstride = pair_x_stride(ks);
+  a.xstride = two_set_x_stride(ks);
   const size_t usable = (size_t)kSmemBudget - 1024;  // minus the base-alignment slack
   if (usable < xbytes + 2 * (size_t)a.stage_bytes) return cudaErrorNotSupported;
   a.stages = (int)((usable - xbytes) / a.stage_bytes);
@@ -672,8 +643,6 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   const int ctas_per_slice = ctx.num_sms / a.nslices > 0 ? ctx.num_sms / a.nslices : 1;
   a.tiles_per_cta = (a.ntiles + ctas_per_slice - 1) / ctas_per_slice;
   int grid = (a.ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta;
-  const unsigned cluster = msets == 2 ? 2u : 1u;  // two row sets run as CTA pairs
-  grid = (grid + (int)cluster - 1) / (int)cluster * (int)cluster;
   a.status = ctx.status;
   a.bias = static_cast<const __half*>(ctx.bias);
   a.bias_mode = ctx.bias_mode;
@@ -692,10 +661,7 @@ cudaError_t launch_smallm_impl(LaunchCtx& ctx, const void* A, int M, const QWeig
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ctx.variant = f32 ? "gemm_smallm_mma16816_f32split" : "gemm_smallm_mma16816";
-  auto launch = [&](dim3 g) {
-    return cluster > 1 ? launch_kernel_clustered(ctx, kern, g, dim3(kThreads), smem, cluster, a, tmap_s)
-                       : launch_kernel(ctx, kern, g, dim3(kThreads), smem, a, tmap_s);
-  };
+  auto launch = [&](dim3 g) { return launch_kernel(ctx, kern, g, dim3(kThreads), smem, a, tmap_s); };
   if (a.nslices == 1) return launch(dim3(grid));
   e = launch(dim3(grid, a.nslices));
   if (e != cudaSuccess) return e;

@@ -111,26 +111,4 @@ cudaError_t launch_kernel(LaunchCtx& ctx, Kern kernel, dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// As launch_kernel, with thread-block clusters of `cluster_x` CTAs along x (grid.x must be
-// a multiple of it).
-template <typename Kern, typename... Args>
-cudaError_t launch_kernel_clustered(LaunchCtx& ctx, Kern kernel, dim3 grid, dim3 block, size_t smem,
-                                    unsigned cluster_x, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = ctx.stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster_x;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = ctx.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
 }  // namespace mnb
