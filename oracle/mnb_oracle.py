@@ -4,35 +4,114 @@ TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's CPU
 baseline leg import this module.  The library itself never calls it, shares no
 code with it, and has no CPU fallback.
 
-What it computes is a plain definition, written out directly:
+The arithmetic is plain C++ with fp64 loops (``oracle/mnb_oracle.cpp``, built by
+``build_native`` with g++ into ``oracle/libmnb_oracle.so``); this module only
+marshals numpy arrays to it and shapes the results.  What it computes:
 
-    Y[m, n] = sum_k A[m, k] * (code[n, k] - zp[n, k // bs]) * scale[n, k // bs]
+    Y[m, n] = sum_k A[m, k] * (code[n, k] - zp[n, g(k)]) * scale[n, g(k)]
 
-with the weight stored in the ONNX ``com.microsoft::MatMulNBits`` layout.
-Sources:
+for a weight in the ONNX ``com.microsoft::MatMulNBits`` layout (onnx-runtime-ep-cuda
+0.1.0-dev.6, ``src/kernels/marlin_gemm.rs``, module doc, section "ONNX MatMulNBits
+int4 format"; onnx-runtime-ep-cuda 0.1.0-dev.3, ``src/kernels/matmul_nbits.rs``,
+kernel ``matmul_nbits_dequant_f32``), summed in ascending ``k``, together with the
+bound ``B[m, n] = sum_k |A[m, k] * w[n, k]|``; a device result ``y`` agrees when
+``|y - Y| <= 2e-3 * B + 1e-5``.
 
-* onnx-runtime-ep-cuda 0.1.0-dev.6, ``src/kernels/marlin_gemm.rs``, module doc,
-  section "ONNX MatMulNBits int4 format": the packed ``[N, k_blocks, bs/2]``
-  byte layout, the low nibble holding the even ``k``, ``[N, k_blocks]`` scales
-  in fp16 or fp32, nibble-packed zero points with ``ceil(k_blocks/2)`` bytes
-  per row, low nibble for the even block, and the default zero point 8.
-* onnx-runtime-ep-cuda 0.1.0-dev.3, ``src/kernels/matmul_nbits.rs``, kernel
-  ``matmul_nbits_dequant_f32``: ``k_blocks = ceil(K/bs)``, the element
-  ``(code - zp) * scale`` written to a ``[K, N]`` fp32 matrix indexed
-  ``depth * N + n``.
-
-Arithmetic is fp64.  Every quantity on the right-hand side is exact in fp64:
-codes and zero points are small integers, fp16 and fp32 scales widen exactly,
-and ``(code - zp) * scale`` has at most 4 + 24 significant bits.  The only
-rounding in ``Y`` is the fp64 summation (done by a BLAS matmul, a library
-primitive), far below the fp16 output precision.
-
-The bound ``B[m, n] = sum_k |A[m, k] * w[n, k]|`` is returned with ``Y``; a
-device result ``y`` agrees when ``|y - Y| <= 2e-3 * B + 1e-5``.
+The products split their output columns over the host's CPUs
+(``os.sched_getaffinity``); each output is still one ascending-k sum, so the
+thread count changes no result.  ``oracle/mnb_oracle_np.py`` is an earlier numpy
+restatement of the same definition, kept as a cross-check.
 """
 from __future__ import annotations
 
+import ctypes
+import os
+import subprocess
+import threading
+
 import numpy as np
+
+_DIR = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_DIR, "mnb_oracle.cpp")
+_LIB_PATH = os.path.join(_DIR, "libmnb_oracle.so")
+_CXXFLAGS = ["-std=c++17", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread"]
+_lock = threading.Lock()
+_lib = None
+
+
+def build_native(force: bool = False) -> str:
+    """Compile ``mnb_oracle.cpp`` into ``libmnb_oracle.so`` when it is missing or older
+    than its source (g++; the same flags on x86-64 and AArch64)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    cxx = os.environ.get("CXX", "g++")
+    tmp = f"{_LIB_PATH}.{os.getpid()}.tmp"
+    r = subprocess.run([cxx, *_CXXFLAGS, _SRC, "-o", tmp], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"building the oracle failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+_P = ctypes.c_void_p
+_LL = ctypes.c_longlong
+_I = ctypes.c_int
+_SIGS = {
+    "orc_k_blocks": (_LL, [_LL, _LL]),
+    "orc_zp_row_bytes": (_LL, [_LL, _LL]),
+    "orc_codes": (None, [_P, _LL, _LL, _LL, _P]),
+    "orc_zero_points": (None, [_P, _LL, _LL, _LL, _P]),
+    "orc_f16_to_f64": (None, [_P, _LL, _P]),
+    "orc_weight_nk": (None, [_P, _P, _I, _P, _P, _LL, _LL, _LL, _P, _I]),
+    "orc_dequant_kn_f32": (None, [_P, _P, _I, _P, _P, _LL, _LL, _LL, _P, _I]),
+    "orc_matmul": (None, [_P, _I, _LL, _P, _P, _I, _P, _P, _LL, _LL, _LL, _P, _P, _I]),
+    "orc_matmul_pairs": (None, [_P, _I, _P, _P, _I, _P, _P, _LL, _LL, _LL, _P, _P, _LL, _P, _P, _I]),
+    "orc_silu": (None, [_P, _LL, _P]),
+    "orc_swiglu": (None, [_P, _P, _LL, _P]),
+    "orc_repacked_bytes": (_LL, [_LL, _LL]),
+    "orc_repack": (None, [_P, _LL, _LL, _LL, _P]),
+    "orc_unrepack_codes": (None, [_P, _LL, _LL, _P]),
+    "orc_act_order_plan": (_LL, [_P, _LL, _LL, _P, _P, _P]),
+    "orc_act_order_prepare": (None, [_P, _P, _I, _P, _LL, _LL, _LL, _P, _P, _LL, _P, _P, _P]),
+    "orc_act_order_gather": (None, [_P, _LL, _LL, _I, _P, _LL, _P]),
+}
+
+
+def lib():
+    """The loaded oracle library (built on first use)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            build_native()
+            h = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(h, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = h
+    return _lib
+
+
+def threads() -> int:
+    """CPUs this process may run on (the oracle's thread count for the products)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover - non-Linux
+        return os.cpu_count() or 1
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u8(a, count, what):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError(f"{what} must be uint8, got {a.dtype}")
+    if a.size != count:
+        raise ValueError(f"{what} has {a.size} bytes, expected {count}")
+    return a.reshape(-1)
+
 
 # ---------------------------------------------------------------------------
 # Storage decoding (layout only, integers)
@@ -40,177 +119,175 @@ import numpy as np
 
 
 def k_blocks(K: int, block_size: int) -> int:
-    """Groups per weight row: ``ceil(K / block_size)`` (matmul_nbits.rs, attribute parsing)."""
-    return -(-K // block_size)
+    """Groups per weight row: ``ceil(K / block_size)``."""
+    return int(lib().orc_k_blocks(K, block_size))
 
 
 def zp_row_bytes(K: int, block_size: int) -> int:
-    """Zero-point bytes per row: ``ceil(k_blocks / 2)`` (marlin_gemm.rs module doc)."""
-    return -(-k_blocks(K, block_size) // 2)
+    """Zero-point bytes per row: ``ceil(k_blocks / 2)``."""
+    return int(lib().orc_zp_row_bytes(K, block_size))
 
 
-def codes(packed: np.ndarray, K: int, N: int, block_size: int) -> np.ndarray:
-    """int64 ``[N, K]`` codes in 0..15.
-
-    The byte for ``(n, k)`` sits at ``(n * k_blocks + k // bs) * (bs / 2) + (k % bs) / 2``;
-    with ``within = k % bs``, an even ``within`` takes the low nibble and an odd one the
-    high nibble (``matmul_nbits_dequant_f32``; marlin_gemm.rs module doc).  Positions of a
-    partial last block beyond ``K`` are never read.
-    """
-    G = k_blocks(K, block_size)
-    blob = block_size // 2
-    flat = np.ascontiguousarray(packed).reshape(-1)
-    if flat.size != N * G * blob:
-        raise ValueError(f"packed has {flat.size} bytes, expected {N * G * blob}")
-    n = np.arange(N, dtype=np.int64)[:, None]
-    k = np.arange(K, dtype=np.int64)[None, :]
-    block = k // block_size
-    within = k - block * block_size
-    byte = flat[(n * G + block) * blob + within // 2].astype(np.int64)
-    return np.where((within & 1) == 1, byte >> 4, byte & 15)
+def _packed(packed, K, N, block_size):
+    return _u8(packed, N * k_blocks(K, block_size) * (block_size // 2), "packed")
 
 
-def zero_points(zp: np.ndarray | None, K: int, N: int, block_size: int) -> np.ndarray:
-    """int64 ``[N, k_blocks]`` zero points.
-
-    ``None`` means the symmetric default 8.  Otherwise the nibble for ``(n, g)`` is in
-    byte ``zp[n * zp_row_bytes + g / 2]``: low nibble for even ``g``, high for odd ``g``.
-    """
-    G = k_blocks(K, block_size)
-    if zp is None:
-        return np.full((N, G), 8, dtype=np.int64)
-    zrb = zp_row_bytes(K, block_size)
-    flat = np.ascontiguousarray(zp).reshape(-1)
-    if flat.size != N * zrb:
-        raise ValueError(f"zero_points has {flat.size} bytes, expected {N * zrb}")
-    n = np.arange(N, dtype=np.int64)[:, None]
-    g = np.arange(G, dtype=np.int64)[None, :]
-    byte = flat[n * zrb + g // 2].astype(np.int64)
-    return np.where((g & 1) == 1, byte >> 4, byte & 15)
+def _zp(zp, K, N, block_size):
+    return None if zp is None else _u8(zp, N * zp_row_bytes(K, block_size), "zero_points")
 
 
-def f16_to_f64(h: np.ndarray) -> np.ndarray:
-    """Exact value of IEEE-754 binary16 numbers, decoded from their bits.
-
-    Normal: (-1)^s * 2^(e-15) * (1 + m/1024); subnormal (e = 0): (-1)^s * 2^-14 * m/1024;
-    e = 31: infinity (m = 0) or NaN.
-    """
-    bits = np.ascontiguousarray(h).view(np.uint16).astype(np.int64)
-    sign = np.where(bits >> 15 == 1, -1.0, 1.0)
-    e = (bits >> 10) & 0x1F
-    m = (bits & 0x3FF).astype(np.float64)
-    normal = np.ldexp(1.0 + m / 1024.0, (e - 15).astype(np.int32))
-    sub = np.ldexp(m / 1024.0, -14)
-    special = np.where(m == 0, np.inf, np.nan)
-    val = np.where(e == 0, sub, np.where(e == 31, special, normal))
-    return sign * val
-
-
-def scales_f64(scales: np.ndarray, K: int, N: int, block_size: int) -> np.ndarray:
-    """``[N, k_blocks]`` scales as exact fp64 (fp16 or fp32 storage)."""
-    G = k_blocks(K, block_size)
+def _scales(scales, K, N, block_size):
     s = np.ascontiguousarray(scales).reshape(-1)
+    G = k_blocks(K, block_size)
     if s.size != N * G:
         raise ValueError(f"scales has {s.size} values, expected {N * G}")
     if s.dtype == np.float16:
-        out = f16_to_f64(s)
-    elif s.dtype == np.float32:
-        out = s.astype(np.float64)
-    else:
-        raise TypeError(f"scales must be float16 or float32, got {s.dtype}")
-    return out.reshape(N, G)
+        return s, 1
+    if s.dtype == np.float32:
+        return s, 0
+    raise TypeError(f"scales must be float16 or float32, got {s.dtype}")
 
 
-# ---------------------------------------------------------------------------
-# The product
-# ---------------------------------------------------------------------------
-
-
-def groups(K: int, block_size: int, g_idx=None) -> np.ndarray:
-    """int64 ``[K]``: the group whose scale and zero point apply at each ``k``.
-
-    Without ``g_idx`` it is the block ``k // bs``.  With the act-order input ``g_idx``
-    (int32 ``[K]`` or ``[k_blocks * bs]``; entries past ``K`` are never read) it is
-    ``g_idx[k]`` (``matmul_nbits_dequant_f32``: ``group = group_indices[depth]``).  The
-    code itself is always read from block ``k // bs``.
-    """
+def _g_idx(g_idx, K, block_size):
+    """int32 ``[K]`` act-order groups (``[K]`` or ``[k_blocks * bs]`` accepted; entries past
+    ``K`` are never read), or None."""
     if g_idx is None:
-        return np.arange(K, dtype=np.int64) // block_size
-    g = np.asarray(g_idx).reshape(-1).astype(np.int64)
+        return None
+    g = np.asarray(g_idx).reshape(-1)
     if g.size not in (K, k_blocks(K, block_size) * block_size):
         raise ValueError(f"g_idx has {g.size} entries, expected {K} or the padded K")
-    return g[:K]
+    return np.ascontiguousarray(g[:K].astype(np.int32))
 
 
-def weight_nk(packed, scales, zp, K: int, N: int, block_size: int, g_idx=None) -> np.ndarray:
-    """Exact fp64 ``w[n, k] = (code[n, k] - zp[n, g]) * scale[n, g]``, ``g = groups(k)``.
-
-    A group outside ``0 .. k_blocks-1`` gives ``w = 0`` (``matmul_nbits_dequant_f32``
-    writes 0 for it; the operator's host check rejects such a ``g_idx`` outright).
-    """
-    c = codes(packed, K, N, block_size)
-    z = zero_points(zp, K, N, block_size)
-    s = scales_f64(scales, K, N, block_size)
-    g = groups(K, block_size, g_idx)
-    ok = (g >= 0) & (g < k_blocks(K, block_size))
-    gc = np.where(ok, g, 0)
-    w = (c - z[:, gc]).astype(np.float64) * s[:, gc]
-    return np.where(ok[None, :], w, 0.0)
+def codes(packed, K: int, N: int, block_size: int) -> np.ndarray:
+    """int64 ``[N, K]`` codes in 0..15 (low nibble for the even ``k`` of a block)."""
+    p = _packed(packed, K, N, block_size)
+    out = np.empty((N, K), dtype=np.int8)
+    lib().orc_codes(_ptr(p), K, N, block_size, _ptr(out))
+    return out.astype(np.int64)
 
 
-def dequant_kn_f32(packed, scales, zp, K: int, N: int, block_size: int, g_idx=None) -> np.ndarray:
-    """fp32 ``[K, N]``: each element is ``(code - zp) * scale`` rounded once to fp32.
-
-    ``matmul_nbits_dequant_f32`` writes this matrix at ``depth * N + n``.  The fp64
-    product is exact, so one rounding gives the correctly rounded fp32 product; for
-    fp16 scales the product is already representable in fp32 and the value is exact.
-    """
-    return weight_nk(packed, scales, zp, K, N, block_size, g_idx).T.astype(np.float32)
+def zero_points(zp, K: int, N: int, block_size: int) -> np.ndarray:
+    """int64 ``[N, k_blocks]`` zero points; ``None`` means the symmetric default 8."""
+    z = _zp(zp, K, N, block_size)
+    out = np.empty((N, k_blocks(K, block_size)), dtype=np.int8)
+    lib().orc_zero_points(_ptr(z), K, N, block_size, _ptr(out))
+    return out.astype(np.int64)
 
 
-def activations_f64(A: np.ndarray) -> np.ndarray:
+def f16_to_f64(h) -> np.ndarray:
+    """Exact fp64 value of IEEE-754 binary16 numbers, decoded from their bits."""
+    h = np.ascontiguousarray(h)
+    bits = h.view(np.uint16).reshape(-1)
+    out = np.empty(bits.size, dtype=np.float64)
+    lib().orc_f16_to_f64(_ptr(bits), bits.size, _ptr(out))
+    return out.reshape(h.shape)
+
+
+def activations_f64(A) -> np.ndarray:
     """Exact fp64 value of fp16 activations (decoded from their bits) or fp32 ones
     (the operator's fp32 path, matmul_nbits.rs: A of type Float32, widened exactly)."""
+    A = np.asarray(A)
     if A.dtype == np.float16:
-        return f16_to_f64(A).reshape(A.shape)
+        return f16_to_f64(A)
     if A.dtype == np.float32:
         return A.astype(np.float64)
     raise TypeError(f"activations are fp16 or fp32, got {A.dtype}")
 
 
-def matmul(A, packed, scales, zp, K: int, N: int, block_size: int, g_idx=None):
+def scales_f64(scales, K: int, N: int, block_size: int) -> np.ndarray:
+    """``[N, k_blocks]`` scales as exact fp64 (fp16 or fp32 storage)."""
+    s, f16 = _scales(scales, K, N, block_size)
+    return (f16_to_f64(s) if f16 else s.astype(np.float64)).reshape(N, k_blocks(K, block_size))
+
+
+# ---------------------------------------------------------------------------
+# Weights and products
+# ---------------------------------------------------------------------------
+
+
+def weight_nk(packed, scales, zp, K: int, N: int, block_size: int, g_idx=None) -> np.ndarray:
+    """Exact fp64 ``w[n, k] = (code[n, k] - zp[n, g]) * scale[n, g]``, ``g = g_idx[k]`` with
+    act-order indices, else ``k // bs``; a group outside ``0 .. k_blocks-1`` gives 0."""
+    p = _packed(packed, K, N, block_size)
+    s, f16 = _scales(scales, K, N, block_size)
+    z = _zp(zp, K, N, block_size)
+    g = _g_idx(g_idx, K, block_size)
+    out = np.empty((N, K), dtype=np.float64)
+    lib().orc_weight_nk(_ptr(p), _ptr(s), f16, _ptr(z), _ptr(g), K, N, block_size, _ptr(out), threads())
+    return out
+
+
+def dequant_kn_f32(packed, scales, zp, K: int, N: int, block_size: int, g_idx=None) -> np.ndarray:
+    """fp32 ``[K, N]``: each element is ``(code - zp) * scale`` rounded once to fp32,
+    at ``depth * N + n`` as ``matmul_nbits_dequant_f32`` writes it."""
+    p = _packed(packed, K, N, block_size)
+    s, f16 = _scales(scales, K, N, block_size)
+    z = _zp(zp, K, N, block_size)
+    g = _g_idx(g_idx, K, block_size)
+    out = np.empty((K, N), dtype=np.float32)
+    lib().orc_dequant_kn_f32(_ptr(p), _ptr(s), f16, _ptr(z), _ptr(g), K, N, block_size, _ptr(out), threads())
+    return out
+
+
+def _acts(A, K):
+    A = np.ascontiguousarray(A)
+    if A.dtype == np.float16:
+        a_f16 = 1
+    elif A.dtype == np.float32:
+        a_f16 = 0
+    else:
+        raise TypeError(f"activations are fp16 or fp32, got {A.dtype}")
+    if A.size % K:
+        raise ValueError(f"activations have {A.size} values, not a multiple of K = {K}")
+    return A.reshape(-1, K), a_f16
+
+
+def matmul(A, packed, scales, zp, K: int, N: int, block_size: int, g_idx=None, nthreads: int | None = None):
     """``(Y, B)``: fp64 ``Y = A . w^T`` and the bound ``B = |A| . |w|^T``, both ``[M, N]``.
 
-    ``A`` is the fp16 activation ``[M, K]`` (taken at its fp16 value, as the pages'
-    oracles consume the same fp16-rounded activations as the kernel).  ``g_idx``: see
-    ``groups``.
+    ``A`` is the fp16 (or fp32) activation ``[M, K]``, taken at its exact value (the pages'
+    oracles consume the same fp16-rounded activations as the kernel).
     """
-    a = activations_f64(A).reshape(-1, K)
-    w = weight_nk(packed, scales, zp, K, N, block_size, g_idx)
-    return a @ w.T, np.abs(a) @ np.abs(w).T
+    a, a_f16 = _acts(A, K)
+    M = a.shape[0]
+    p = _packed(packed, K, N, block_size)
+    s, f16 = _scales(scales, K, N, block_size)
+    z = _zp(zp, K, N, block_size)
+    g = _g_idx(g_idx, K, block_size)
+    Y = np.empty((M, N), dtype=np.float64)
+    B = np.empty((M, N), dtype=np.float64)
+    lib().orc_matmul(_ptr(a), a_f16, M, _ptr(p), _ptr(s), f16, _ptr(z), _ptr(g), K, N, block_size,
+                     _ptr(Y), _ptr(B), nthreads or threads())
+    return Y, B
 
 
 def matmul_rows(A, packed, scales, zp, K: int, N: int, block_size: int, rows, cols, g_idx=None):
-    """``(Y, B)`` at the listed ``(row, col)`` pairs only (full-size spot checks)."""
-    rows = np.asarray(rows, dtype=np.int64)
-    cols = np.asarray(cols, dtype=np.int64)
-    a = activations_f64(A).reshape(-1, K)
-    ucols, inv = np.unique(cols, return_inverse=True)
-    G = k_blocks(K, block_size)
-    blob = block_size // 2
-    sub_packed = np.ascontiguousarray(packed).reshape(N, G * blob)[ucols]
-    sub_scales = np.ascontiguousarray(scales).reshape(N, G)[ucols]
-    sub_zp = None if zp is None else np.ascontiguousarray(zp).reshape(N, -1)[ucols]
-    w = weight_nk(sub_packed, sub_scales, sub_zp, K, len(ucols), block_size, g_idx)
-    ar = a[rows]
-    wc = w[inv]
-    return np.einsum("ik,ik->i", ar, wc), np.einsum("ik,ik->i", np.abs(ar), np.abs(wc))
+    """``(Y, B)`` at the listed ``(rows[i], cols[i])`` pairs only (1-D, one per pair)."""
+    a, a_f16 = _acts(A, K)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64).reshape(-1))
+    if rows.size != cols.size:
+        raise ValueError("rows and cols differ in length")
+    if rows.size and (rows.min() < 0 or rows.max() >= a.shape[0] or cols.min() < 0 or cols.max() >= N):
+        raise ValueError("a (row, col) pair is outside the output")
+    p = _packed(packed, K, N, block_size)
+    s, f16 = _scales(scales, K, N, block_size)
+    z = _zp(zp, K, N, block_size)
+    g = _g_idx(g_idx, K, block_size)
+    Y = np.empty(rows.size, dtype=np.float64)
+    B = np.empty(rows.size, dtype=np.float64)
+    lib().orc_matmul_pairs(_ptr(a), a_f16, _ptr(p), _ptr(s), f16, _ptr(z), _ptr(g), K, N, block_size,
+                           _ptr(rows), _ptr(cols), rows.size, _ptr(Y), _ptr(B), threads())
+    return Y, B
 
 
-def silu(x: np.ndarray) -> np.ndarray:
+def silu(x) -> np.ndarray:
     """``x / (1 + exp(-x))`` in fp64."""
-    with np.errstate(over="ignore"):
-        return x / (1.0 + np.exp(-x))
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty_like(x)
+    lib().orc_silu(_ptr(x), x.size, _ptr(out))
+    return out
 
 
 def gate_up_swiglu(A, gate, up, K: int, N: int, block_size: int):
@@ -222,7 +299,9 @@ def gate_up_swiglu(A, gate, up, K: int, N: int, block_size: int):
     """
     g, bg = matmul(A, *gate, K, N, block_size)
     u, bu = matmul(A, *up, K, N, block_size)
-    return silu(g) * u, g, bg, u, bu
+    out = np.empty_like(g)
+    lib().orc_swiglu(_ptr(g), _ptr(u), g.size, _ptr(out))
+    return out, g, bg, u, bu
 
 
 def swiglu_tolerance(g, bg, u, bu, out_ref):
@@ -240,83 +319,33 @@ def swiglu_tolerance(g, bg, u, bu, out_ref):
 
 
 # ---------------------------------------------------------------------------
-# The repacked tensor-core operand layout
+# The repacked tensor-core operand layout (specification in mnb_oracle.cpp)
 # ---------------------------------------------------------------------------
-#
-# This layout is this library's own (the pages repack for mma.sync fragments; the
-# layout here is built for 1-D bulk copies and shared-memory dequantisation):
-#
-#   Np = ceil(N / 128) * 128, Kp = ceil(K / 64) * 64, size = Np * Kp / 2 bytes.
-#   Tile t (128 rows) and k-block b (64 k) form one 4096-byte block at byte
-#   (t * (Kp / 64) + b) * 4096.  Inside it, the 16 bytes at q * 2048 + r * 16
-#   (q in 0..1, r in 0..127) hold the 32 codes of row n = 128 t + r for
-#   k = 64 b + 32 q + i, i in 0..31.  Those 16 bytes are four little-endian 32-bit
-#   words; word j = i // 8 holds i at nibble position p (bits 4p..4p+3) where
-#   i = 8 j + 2 (p % 4) + p // 4.  Codes for n >= N or k >= K are 0.
-#
-# Nothing here is shared with the device code; this is an independent restatement
-# of the same specification.
-
-REPACK_TILE_N = 128
-REPACK_TILE_K = 64
 
 
 def repacked_bytes(K: int, N: int) -> int:
-    np_ = -(-N // REPACK_TILE_N) * REPACK_TILE_N
-    kp = -(-K // REPACK_TILE_K) * REPACK_TILE_K
-    return np_ * kp // 2
-
-
-def _repack_positions(K: int, N: int):
-    """For every (n, k): destination byte and nibble half (0 low, 1 high)."""
-    kp = -(-K // REPACK_TILE_K) * REPACK_TILE_K
-    n = np.arange(N, dtype=np.int64)[:, None]
-    k = np.arange(K, dtype=np.int64)[None, :]
-    t, r = n // REPACK_TILE_N, n % REPACK_TILE_N
-    b, kk = k // REPACK_TILE_K, k % REPACK_TILE_K
-    q, i = kk // 32, kk % 32
-    j, i8 = i // 8, i % 8
-    # invert i8 = 2 (p % 4) + p // 4
-    p = (i8 // 2) + 4 * (i8 % 2)
-    byte = (t * (kp // REPACK_TILE_K) + b) * 4096 + q * 2048 + r * 16 + 4 * j + p // 2
-    return byte, np.broadcast_to(p % 2, byte.shape)
+    return int(lib().orc_repacked_bytes(K, N))
 
 
 def repack(packed, K: int, N: int, block_size: int) -> np.ndarray:
     """uint8 repacked buffer of ``repacked_bytes(K, N)`` bytes."""
-    c = codes(packed, K, N, block_size)
-    byte, half = _repack_positions(K, N)
-    out = np.zeros(repacked_bytes(K, N), dtype=np.uint8)
-    lo = half == 0
-    out[byte[lo]] |= c[lo].astype(np.uint8)
-    out[byte[~lo]] |= (c[~lo] << 4).astype(np.uint8)
+    p = _packed(packed, K, N, block_size)
+    out = np.empty(repacked_bytes(K, N), dtype=np.uint8)
+    lib().orc_repack(_ptr(p), K, N, block_size, _ptr(out))
     return out
 
 
-def unrepack_codes(repacked: np.ndarray, K: int, N: int) -> np.ndarray:
+def unrepack_codes(repacked, K: int, N: int) -> np.ndarray:
     """int64 ``[N, K]`` codes read back from a repacked buffer."""
-    byte, half = _repack_positions(K, N)
-    v = np.asarray(repacked).reshape(-1)[byte].astype(np.int64)
-    return np.where(half == 1, v >> 4, v & 15)
+    r = _u8(repacked, repacked_bytes(K, N), "repacked")
+    out = np.empty((N, K), dtype=np.int8)
+    lib().orc_unrepack_codes(_ptr(r), K, N, _ptr(out))
+    return out.astype(np.int64)
 
 
 # ---------------------------------------------------------------------------
-# Act-order weights prepared for the block kernels
+# Act-order weights prepared for the block kernels (plan in mnb_oracle.cpp)
 # ---------------------------------------------------------------------------
-#
-# With ``g_idx`` the members of a group are scattered over K.  Reordering k so that
-# each group's members sit together turns the weight into a plain block weight:
-#
-#   * groups in ascending order; inside a group, its members in ascending k;
-#   * each group's run padded with empty slots (-1) to a whole number of blocks;
-#   * ``perm[k']`` = the source k of prepared position k' (or -1), ``K' = len(perm)``,
-#     ``block_group[j]`` = the group of prepared block j.
-#
-# The prepared weight has codes ``code[n, perm[k']]`` (the block's zero point at an
-# empty slot, so its weight is 0), and the scale and zero point of ``block_group[j]``
-# for block j.  The matching activation is ``A'[m, k'] = A[m, perm[k']]`` (0 at an
-# empty slot), and ``A' . w'^T = A . w^T`` term by term.  This preparation is this
-# library's own; the pages dequantise with ``g_idx`` directly.
 
 
 def act_order_plan(g_idx, K: int, block_size: int):
@@ -325,26 +354,16 @@ def act_order_plan(g_idx, K: int, block_size: int):
     Raises ``ValueError`` for an entry outside ``0 .. k_blocks-1`` (the operator's own
     check on ``g_idx``, matmul_nbits.rs).
     """
+    g = _g_idx(g_idx, K, block_size)
     G = k_blocks(K, block_size)
-    g = groups(K, block_size, g_idx)
-    bad = np.nonzero((g < 0) | (g >= G))[0]
-    if bad.size:
-        raise ValueError(f"g_idx[{bad[0]}]={g[bad[0]]} is outside 0..{G}")
-    perm, block_group = [], []
-    for grp in range(G):
-        members = np.nonzero(g == grp)[0].tolist()
-        nblocks = -(-len(members) // block_size)
-        perm += members + [-1] * (nblocks * block_size - len(members))
-        block_group += [grp] * nblocks
-    return len(perm), np.array(perm, dtype=np.int32), np.array(block_group, dtype=np.int32)
-
-
-def _pack_nibbles(v: np.ndarray) -> np.ndarray:
-    """uint8 rows from int rows of 4-bit values: low nibble from the even position."""
-    v = np.asarray(v, dtype=np.int64)
-    if v.shape[1] % 2:
-        v = np.concatenate([v, np.zeros((v.shape[0], 1), dtype=np.int64)], axis=1)
-    return (v[:, 0::2] | (v[:, 1::2] << 4)).astype(np.uint8)
+    cap = K + G * (block_size - 1)
+    perm = np.empty(cap, dtype=np.int32)
+    bg = np.empty(cap // block_size + 1, dtype=np.int32)
+    bad = ctypes.c_longlong(-1)
+    kp = int(lib().orc_act_order_plan(_ptr(g), K, block_size, _ptr(perm), _ptr(bg), ctypes.byref(bad)))
+    if kp < 0:
+        raise ValueError(f"g_idx[{bad.value}]={int(g[bad.value])} is outside 0..{G}")
+    return kp, perm[:kp].copy(), bg[: kp // block_size].copy()
 
 
 def act_order_prepare(packed, scales, zp, K: int, N: int, block_size: int, perm, block_group):
@@ -354,27 +373,32 @@ def act_order_prepare(packed, scales, zp, K: int, N: int, block_size: int, perm,
     ``[N, K'/bs]``, ``zero_points'`` is uint8 ``[N, ceil(K'/bs/2)]`` (the unused high
     nibble of an odd count is 0), or ``None`` when the weight has none.
     """
-    perm = np.asarray(perm, dtype=np.int64)
-    bg = np.asarray(block_group, dtype=np.int64)
+    perm = np.ascontiguousarray(np.asarray(perm, dtype=np.int32).reshape(-1))
+    bg = np.ascontiguousarray(np.asarray(block_group, dtype=np.int32).reshape(-1))
     Kp = perm.size
     if Kp % block_size or bg.size != Kp // block_size:
         raise ValueError("perm and block_group do not describe whole blocks")
-    c = codes(packed, K, N, block_size)
-    z = zero_points(zp, K, N, block_size)
-    zb = z[:, bg]                                         # [N, K'/bs]
-    zk = zb[:, np.arange(Kp) // block_size]               # [N, K']
-    cp = np.where(perm[None, :] >= 0, c[:, np.maximum(perm, 0)], zk)
-    G = k_blocks(K, block_size)
-    sp = np.ascontiguousarray(scales).reshape(N, G)[:, bg].copy()
-    zpp = None if zp is None else _pack_nibbles(zb)
-    return _pack_nibbles(cp), sp, zpp
+    p = _packed(packed, K, N, block_size)
+    s, _ = _scales(scales, K, N, block_size)
+    z = _zp(zp, K, N, block_size)
+    Gp = Kp // block_size
+    pk = np.empty((N, Kp // 2), dtype=np.uint8)
+    sp = np.empty((N, Gp), dtype=s.dtype)
+    zpp = None if z is None else np.empty((N, (Gp + 1) // 2), dtype=np.uint8)
+    lib().orc_act_order_prepare(_ptr(p), _ptr(s), s.itemsize, _ptr(z), K, N, block_size, _ptr(perm), _ptr(bg), Kp,
+                                _ptr(pk), _ptr(sp), _ptr(zpp))
+    return pk, sp, zpp
 
 
 def act_order_gather(A, perm) -> np.ndarray:
-    """fp16 ``A'[m, k'] = A[m, perm[k']]``, and +0 where ``perm[k'] = -1``."""
-    A = np.asarray(A)
-    perm = np.asarray(perm, dtype=np.int64)
-    out = np.zeros((A.shape[0], perm.size), dtype=A.dtype)
-    ok = perm >= 0
-    out[:, ok] = A[:, perm[ok]]
+    """``A'[m, k'] = A[m, perm[k']]``, and +0 where ``perm[k'] = -1`` (same dtype as A)."""
+    A = np.ascontiguousarray(A)
+    if A.ndim == 1:
+        A = A.reshape(1, -1)
+    perm = np.ascontiguousarray(np.asarray(perm, dtype=np.int32).reshape(-1))
+    M, K = A.shape
+    if perm.size and perm.max() >= K:
+        raise ValueError("perm names a column past K")
+    out = np.empty((M, perm.size), dtype=A.dtype)
+    lib().orc_act_order_gather(_ptr(A), M, K, A.itemsize, _ptr(perm), perm.size, _ptr(out))
     return out

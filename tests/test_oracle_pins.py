@@ -1,4 +1,5 @@
-"""Pins for the fp64 oracle: each checks it against something other than itself.
+"""Pins for the fp64 oracle (C++ loops in oracle/mnb_oracle.cpp, loaded through
+oracle/mnb_oracle.py): each checks it against something other than itself.
 
 * a hand-decoded worked example of the storage (tests/golden),
 * single-hot brute force on every block size (pins the (n, k) -> byte/nibble map),
@@ -15,7 +16,12 @@
 * act-order ``g_idx``: the identity reduces to the plain layout; a weight built the
   act-order way (codes quantised in a visit order, stored in k order) dequantises to
   the same matrix; exact rational brute force with uneven and out-of-range groups;
-  a hand-worked preparation plan; the prepared weight holds the same weights.
+  a hand-worked preparation plan; the prepared weight holds the same weights,
+* the spot-check product at (row, col) pairs equals the full product there, with
+  repeated and unsorted pairs, act-order groups and fp32 activations,
+* the thread count changes no result,
+* the C++ oracle agrees with an earlier numpy restatement (integers and fp32 dequant
+  bitwise, Y to fp64 summation order).
 """
 from __future__ import annotations
 
@@ -289,14 +295,24 @@ def test_repack_roundtrip_is_bijection(bs):
     rp = orc.repack(packed, K, N, bs)
     assert rp.size == orc.repacked_bytes(K, N)
     np.testing.assert_array_equal(orc.unrepack_codes(rp, K, N), orc.codes(packed, K, N, bs))
-    # every stored nibble used exactly once; padding nibbles are zero
-    byte, half = orc._repack_positions(K, N)
-    slots = byte * 2 + half
-    assert np.unique(slots).size == slots.size
-    mask = np.ones(rp.size * 2, dtype=bool)
-    mask[slots.reshape(-1)] = False
-    nibbles = np.stack([rp & 15, rp >> 4], axis=1).reshape(-1)
-    assert np.all(nibbles[mask] == 0)
+    # every stored nibble used exactly once, padding nibbles zero: with every code 15 the
+    # buffer holds exactly N * K set nibbles (two codes sent to one nibble would leave
+    # fewer), and each single-hot code lands alone
+    full = orc.repack(np.full((N, K // 2), 0xFF, dtype=np.uint8), K, N, bs)
+    nib = np.stack([full & 15, full >> 4], axis=1).reshape(-1)
+    assert set(np.unique(nib).tolist()) <= {0, 15}
+    assert int(np.count_nonzero(nib)) == N * K
+    rng = np.random.default_rng(bs)
+    seen = set()
+    for _ in range(64):
+        n, k = int(rng.integers(N)), int(rng.integers(K))
+        c = np.zeros((N, K), dtype=np.int64)
+        c[n, k] = 9
+        one = orc.repack(_pack_codes(c), K, N, bs)
+        nz = np.nonzero(one)[0]
+        assert nz.size == 1 and one[nz[0]] in (0x09, 0x90)
+        seen.add((int(nz[0]), int(one[nz[0]]), n, k))
+    assert len({(b, v) for b, v, _, _ in seen}) == len({(n, k) for _, _, n, k in seen})
 
 
 def test_synth_streams_are_deterministic():
@@ -465,3 +481,89 @@ def test_f32_activations_exact_rational():
     Y32, _ = orc.matmul(A, packed, scales, zp, K, N, bs)
     Y16, _ = orc.matmul(A.astype(np.float16), packed, scales, zp, K, N, bs)
     assert not np.allclose(Y16, Y32, rtol=1e-9, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# Spot-check products, thread-count invariance, and the numpy cross-check
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("case", ["zp_f16", "nozp_f32", "gidx_uneven", "gidx_act_order", "f32_act"])
+def test_matmul_rows_equals_matmul_at_the_pairs(case):
+    """The spot-check product at (row, col) pairs (the full-size referee) equals the full
+    product there bit for bit, with repeated and unsorted columns and rows, with and
+    without zero points, fp16 and fp32 scales, with act-order groups (uneven sizes, some
+    empty) and fp32 activations."""
+    sdt = "f32" if case == "nozp_f32" else "f16"
+    wl = syn.custom(f"pin_rows_{case}", 5, 384, 37, 32, scales_dtype=sdt, has_zp=case != "nozp_f32")
+    w = syn.make_weight(wl)
+    A = syn.make_activation_f32(wl) if case == "f32_act" else syn.make_activation(wl)
+    g_idx = None
+    if case.startswith("gidx"):
+        g_idx = syn.make_g_idx(wl, "uneven" if case == "gidx_uneven" else "act_order")
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size, g_idx)
+    rows = np.array([4, 0, 4, 2, 1, 3, 0, 4, 2, 2], dtype=np.int64)
+    cols = np.array([36, 5, 5, 0, 36, 17, 17, 2, 2, 30], dtype=np.int64)
+    y, b = orc.matmul_rows(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size, rows, cols, g_idx)
+    np.testing.assert_array_equal(y, Y[rows, cols])
+    np.testing.assert_array_equal(b, B[rows, cols])
+
+
+def test_matmul_rows_sees_the_column_of_each_pair():
+    """Two pairs at one row and two columns with different weights give the two different
+    full-product values (a mapping that sent every pair to one column would not)."""
+    wl = syn.custom("pin_rows_cols", 2, 128, 4, 32)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    Y, _ = orc.matmul(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size)
+    y, _ = orc.matmul_rows(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size, [1, 1, 0], [3, 0, 3])
+    assert len({float(v) for v in Y[[1, 1, 0], [3, 0, 3]]}) == 3
+    np.testing.assert_array_equal(y, Y[[1, 1, 0], [3, 0, 3]])
+
+
+def test_matmul_thread_count_changes_nothing():
+    wl = syn.custom("pin_threads", 3, 512, 67, 64)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    Y1, B1 = orc.matmul(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size, nthreads=1)
+    Y7, B7 = orc.matmul(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size, nthreads=7)
+    np.testing.assert_array_equal(Y1, Y7)
+    np.testing.assert_array_equal(B1, B7)
+
+
+@pytest.mark.parametrize("bs,sdt,has_zp,gkind", [(16, "f16", True, None), (32, "f32", False, None),
+                                                  (64, "f16", True, "uneven"), (128, "f32", True, "act_order")])
+def test_cpp_oracle_agrees_with_numpy_restatement(bs, sdt, has_zp, gkind):
+    """The C++ oracle and the earlier numpy restatement of the same definition: integer
+    decodes, the fp32 dequant and the repack byte for byte; Y to fp64 summation order."""
+    from oracle import mnb_oracle_np as onp
+    wl = syn.custom(f"pin_xcheck_{bs}_{sdt}", 3, 4 * max(bs, 64), 29, bs, scales_dtype=sdt, has_zp=has_zp)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    K, N = wl.K, wl.N
+    g_idx = None if gkind is None else syn.make_g_idx(wl, gkind)
+    np.testing.assert_array_equal(orc.codes(w.packed, K, N, bs), onp.codes(w.packed, K, N, bs))
+    np.testing.assert_array_equal(orc.zero_points(w.zero_points, K, N, bs), onp.zero_points(w.zero_points, K, N, bs))
+    np.testing.assert_array_equal(orc.weight_nk(w.packed, w.scales, w.zero_points, K, N, bs, g_idx),
+                                  onp.weight_nk(w.packed, w.scales, w.zero_points, K, N, bs, g_idx))
+    np.testing.assert_array_equal(orc.dequant_kn_f32(w.packed, w.scales, w.zero_points, K, N, bs, g_idx).view(np.uint32),
+                                  onp.dequant_kn_f32(w.packed, w.scales, w.zero_points, K, N, bs, g_idx).view(np.uint32))
+    np.testing.assert_array_equal(orc.repack(w.packed, K, N, bs), onp.repack(w.packed, K, N, bs))
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs, g_idx)
+    Yn, Bn = onp.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs, g_idx)
+    assert np.all(np.abs(Y - Yn) <= 1e-12 * B)
+    np.testing.assert_allclose(B, Bn, rtol=1e-12, atol=0)
+    if g_idx is not None:
+        plan, plan_n = orc.act_order_plan(g_idx, K, bs), onp.act_order_plan(g_idx, K, bs)
+        assert plan[0] == plan_n[0]
+        np.testing.assert_array_equal(plan[1], plan_n[1])
+        np.testing.assert_array_equal(plan[2], plan_n[2])
+        prep = orc.act_order_prepare(w.packed, w.scales, w.zero_points, K, N, bs, plan[1], plan[2])
+        prep_n = onp.act_order_prepare(w.packed, w.scales, w.zero_points, K, N, bs, plan[1], plan[2])
+        for x, xn in zip(prep, prep_n):
+            if x is None:
+                assert xn is None
+            else:
+                np.testing.assert_array_equal(x.view(np.uint8), xn.view(np.uint8))
+        np.testing.assert_array_equal(orc.act_order_gather(A, plan[1]).view(np.uint16),
+                                      onp.act_order_gather(A, plan[1]).view(np.uint16))
