@@ -101,11 +101,13 @@ mnb_status make_ctx(const char* fn, mnb_stream stream, mnb::LaunchCtx* ctx) {
   return MNB_OK;
 }
 
-// M = 1: the bulk-copy ring kernel when rows are 16-byte multiples, else the
-// register-pipelined kernel, else the generic kernel.
+// M = 1: the tensor-core streaming kernel (K % 256 == 0, block size 32/64/128), else the
+// bulk-copy ring kernel when rows are 16-byte multiples, else the register-pipelined
+// kernel, else the generic kernel.
 cudaError_t run_gemv(mnb::LaunchCtx& ctx, const void* A, const mnb::QWeight& q, int K, int N, int bs,
                      void* Y) {
-  cudaError_t e = mnb::launch_gemv_tma(ctx, A, q, K, N, bs, Y);
+  cudaError_t e = mnb::launch_gemv_mma(ctx, A, q, K, N, bs, Y);
+  if (e == cudaErrorNotSupported) e = mnb::launch_gemv_tma(ctx, A, q, K, N, bs, Y);
   if (e == cudaErrorNotSupported) e = mnb::launch_gemv(ctx, A, q, K, N, bs, Y);
   if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, 1, q, K, N, bs, Y);
   return e;
@@ -297,7 +299,8 @@ mnb_status mnb_gemv_gate_up_swiglu(const void* A, mnb_weight gate, mnb_weight up
   if ((st = check_ptr(fn, "out", out)) != MNB_OK) return st;
   mnb::LaunchCtx ctx;
   if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
-  cudaError_t e = mnb::launch_gemv_pair_swiglu_tma(ctx, A, g, u, K, N, block_size, out);
+  cudaError_t e = mnb::launch_gemv_pair_swiglu_mma(ctx, A, g, u, K, N, block_size, out);
+  if (e == cudaErrorNotSupported) e = mnb::launch_gemv_pair_swiglu_tma(ctx, A, g, u, K, N, block_size, out);
   if (e == cudaErrorNotSupported) e = mnb::launch_gemv_pair_swiglu(ctx, A, g, u, K, N, block_size, out);
   if (e == cudaErrorNotSupported) e = mnb::launch_generic_pair_swiglu(ctx, A, g, u, K, N, block_size, out);
   return finish(fn, e, ctx);

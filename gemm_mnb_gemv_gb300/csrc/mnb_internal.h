@@ -47,6 +47,11 @@ cudaError_t launch_gemv_tma(LaunchCtx& ctx, const void* A, const QWeight& w, int
                             void* Y);
 cudaError_t launch_gemv_pair_swiglu_tma(LaunchCtx& ctx, const void* A, const QWeight& gate,
                                         const QWeight& up, int K, int N, int bs, void* out);
+// M = 1 GEMV with the multiply-accumulate on mma.sync tensor cores (K % 256 == 0, block
+// size 32/64/128); cudaErrorNotSupported for other shapes.
+cudaError_t launch_gemv_mma(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs, void* Y);
+cudaError_t launch_gemv_pair_swiglu_mma(LaunchCtx& ctx, const void* A, const QWeight& gate, const QWeight& up,
+                                        int K, int N, int bs, void* out);
 // Register-pipelined M = 1 GEMV; cudaErrorNotSupported when the shape has no variant.
 cudaError_t launch_gemv(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs,
                         void* Y);

@@ -71,26 +71,36 @@ def test_repack_bit_exact(env, K, N, bs):
 
 
 GEMV_CASES = [
-    # name, K, N, bs, scales, zp, act  -- chosen to hit every fast-GEMV geometry
-    ("gv_one_col", 64, 1, 16, "f16", True, "normal"),
-    ("gv_ragged32", 96, 130, 32, "f16", True, "normal"),
-    ("gv_ragged64", 192, 200, 64, "f32", False, "normal"),
-    ("gv_bs128", 384, 333, 128, "f32", True, "normal"),
-    ("gv_bs16_mid", 2048, 301, 16, "f16", True, "normal"),
-    ("gv_k8192", 8192, 300, 64, "f16", True, "normal"),
-    ("gv_k16384", 16384, 100, 32, "f32", True, "normal"),
-    ("gv_k32768", 32768, 70, 128, "f16", False, "normal"),
-    ("gv_generic_k48", 48, 5, 16, "f16", True, "normal"),
-    ("gv_generic_k65536", 65536, 9, 64, "f16", True, "normal"),
-    # zero-point rows that are not 16-byte multiples (4, 28, 56 bytes): read from global
-    ("gv_zrow4", 1024, 150, 128, "f16", True, "normal"),
-    ("gv_zrow28", 3584, 200, 64, "f32", True, "normal"),
-    ("gv_zrow56_down", 14336, 1000, 128, "f16", True, "normal"),
+    # name, K, N, bs, scales, zp, act, expected kernel (None: not asserted) -- chosen to hit
+    # every M = 1 geometry: the tensor-core streaming kernel (K % 256 == 0, bs >= 32; half-SM
+    # CTAs with all stages in flight, whole-K stages on a full SM, K slices), the bulk-copy
+    # ring kernel, the register-pipelined kernel and the generic kernel
+    ("gv_one_col", 64, 1, 16, "f16", True, "normal", "gemv_f16acc32"),
+    ("gv_ragged32", 96, 130, 32, "f16", True, "normal", "gemv_f16acc32"),
+    ("gv_ragged64", 192, 200, 64, "f32", False, "normal", None),
+    ("gv_bs128", 384, 333, 128, "f32", True, "normal", None),
+    ("gv_bs16_mid", 2048, 301, 16, "f16", True, "normal", "gemv_tma_ring"),
+    ("gv_k8192", 8192, 300, 64, "f16", True, "normal", "gemv_mma"),
+    ("gv_k16384", 16384, 100, 32, "f32", True, "normal", "gemv_tma_ring"),  # zero points, no K slices
+    ("gv_k32768", 32768, 70, 128, "f16", False, "normal", "gemv_mma"),  # four K slices
+    ("gv_generic_k48", 48, 5, 16, "f16", True, "normal", "generic"),
+    ("gv_generic_k65536", 65536, 9, 64, "f16", True, "normal", "generic"),
+    # zero-point rows that are not 16-byte multiples (4, 28, 56 bytes)
+    ("gv_zrow4", 1024, 150, 128, "f16", True, "normal", "gemv_tma_ring"),  # read from global
+    ("gv_zrow28", 3584, 200, 64, "f32", True, "normal", "gemv_mma"),  # 16-row tiles copy whole
+    ("gv_zrow56_down", 14336, 1000, 128, "f16", True, "normal", "gemv_tma_ring"),
+    # the tensor-core kernel: ragged last tile with zero points, fp32 scales, several tiles
+    # per CTA, K slices on the down-projection shape
+    ("gv_mma_ragged_zp", 1024, 1000, 32, "f16", True, "normal", "gemv_mma"),
+    ("gv_mma_bs64_f32", 2048, 333, 64, "f32", False, "normal", "gemv_mma"),
+    ("gv_mma_bs128_multi", 4096, 3001, 128, "f16", True, "normal", "gemv_mma"),
+    ("gv_mma_sliced_f32", 14336, 517, 32, "f32", False, "normal", "gemv_mma"),
+    ("gv_mma_one_tile", 256, 16, 32, "f16", True, "normal", "gemv_mma"),
 ]
 
 
-@pytest.mark.parametrize("name,K,N,bs,sdt,zp,act", GEMV_CASES)
-def test_gemv_parity(env, name, K, N, bs, sdt, zp, act):
+@pytest.mark.parametrize("name,K,N,bs,sdt,zp,act,kernel", GEMV_CASES)
+def test_gemv_parity(env, name, K, N, bs, sdt, zp, act, kernel):
     mnb, torch, dev = env
     wl = syn.custom(name, 1, K, N, bs, scales_dtype=sdt, has_zp=zp, act=act)
     w = syn.make_weight(wl)
@@ -100,12 +110,8 @@ def test_gemv_parity(env, name, K, N, bs, sdt, zp, act):
     torch.cuda.synchronize()
     Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
     assert_within_bound(y.cpu().numpy()[None, :], Y, B, name)
-    expect_generic = (K % 32 != 0) or K > 32768
-    assert variant.startswith("generic") == expect_generic, variant
-    if name in ("gv_one_col", "gv_ragged32"):  # scale rows of 8 and 6 bytes
-        assert variant == "gemv_f16acc32", variant
-    if name.startswith("gv_zrow"):
-        assert variant == "gemv_tma_ring", variant
+    if kernel is not None:
+        assert variant == kernel or (kernel == "generic" and variant.startswith("generic")), variant
 
 
 @pytest.mark.parametrize("wname", ["tiny_gemv_k256_n128", "gemv_attnproj_k4096_n4096",
@@ -121,17 +127,20 @@ def test_gemv_workloads_full_size(env, wname):
     assert_within_bound(y.cpu().numpy()[None, :], Y, B, wname)
 
 
-def _swiglu_case(env, wl):
+def _swiglu_case(env, wl, kernel=None):
     mnb, torch, dev = env
     wg = syn.make_weight(wl, "gate")
     wu = syn.make_weight(wl, "up")
     A = syn.make_activation(wl)
     out = mnb.mnb_gemv_gate_up_swiglu(upload_act(A.reshape(-1), dev), upload_weight(wg, dev),
                                       upload_weight(wu, dev), wl.K, wl.N, wl.block_size)
+    variant = mnb.mnb_last_variant()
     torch.cuda.synchronize()
     ref, g, bg, u, bu = orc.gate_up_swiglu(A, (wg.packed, wg.scales, wg.zero_points),
                                            (wu.packed, wu.scales, wu.zero_points),
                                            wl.K, wl.N, wl.block_size)
+    if kernel is not None:
+        assert variant == kernel, variant
     tol = orc.swiglu_tolerance(g, bg, u, bu, ref)
     got = out.cpu().numpy().astype(np.float64)[None, :]
     assert np.all(np.isfinite(got))
@@ -143,10 +152,15 @@ def test_gate_up_swiglu_workload_full_size(env):
     _swiglu_case(env, syn.WORKLOADS["mlp_gate_up_k4096_n14336"])
 
 
-@pytest.mark.parametrize("K,N,bs,sdt,zp", [(256, 130, 32, "f16", True), (1024, 77, 16, "f32", False),
-                                           (8192, 65, 64, "f16", True), (48, 9, 16, "f16", True)])
-def test_gate_up_swiglu_ragged(env, K, N, bs, sdt, zp):
-    _swiglu_case(env, syn.custom(f"sw_{K}_{N}_{bs}", 1, K, N, bs, scales_dtype=sdt, has_zp=zp))
+@pytest.mark.parametrize("K,N,bs,sdt,zp,kernel", [
+    (256, 130, 32, "f16", True, None), (1024, 77, 16, "f32", False, None),
+    (8192, 65, 64, "f16", True, None), (48, 9, 16, "f16", True, None),
+    # the tensor-core pair kernel: half-SM CTAs, zero points with a ragged tile, K slices
+    (2048, 333, 64, "f32", False, "gemv_pair_swiglu_mma"),
+    (4096, 1000, 128, "f16", True, "gemv_pair_swiglu_mma"),
+    (14336, 100, 32, "f32", False, "gemv_pair_swiglu_mma")])
+def test_gate_up_swiglu_ragged(env, K, N, bs, sdt, zp, kernel):
+    _swiglu_case(env, syn.custom(f"sw_{K}_{N}_{bs}", 1, K, N, bs, scales_dtype=sdt, has_zp=zp), kernel)
 
 
 @pytest.mark.parametrize("M", [2, 4, 8, 16])
@@ -446,12 +460,11 @@ def test_programmatic_launch_gives_same_bits(env):
         assert torch.equal(b, p)
 
 
-# tiny_gemv: 4-byte zero-point rows, read from global by the streaming kernel; the
-# register-pipelined kernel still takes scale rows that are not 16-byte multiples
-# (gv_one_col, gv_ragged32 in GEMV_CASES).
-@pytest.mark.parametrize("wname,variant", [("gemv_attnproj_k4096_n4096", "gemv_tma_ring"),
-                                           ("mlp_down_k14336_n4096", "gemv_tma_ring"),
-                                           ("tiny_gemv_k256_n128", "gemv_tma_ring")])
+# Every M = 1 workload runs on the tensor-core streaming kernel (tiny_gemv's 4-byte
+# zero-point rows copy whole with its 16-row tiles).
+@pytest.mark.parametrize("wname,variant", [("gemv_attnproj_k4096_n4096", "gemv_mma"),
+                                           ("mlp_down_k14336_n4096", "gemv_mma"),
+                                           ("tiny_gemv_k256_n128", "gemv_mma")])
 def test_gemv_dispatch_picks_the_streaming_kernel(env, wname, variant):
     mnb, torch, dev = env
     wl = syn.WORKLOADS[wname]
@@ -468,7 +481,7 @@ def test_swiglu_dispatch_picks_the_streaming_kernel(env):
     wu = upload_weight(syn.make_weight(wl, "up"), dev)
     a = upload_act(syn.make_activation(wl).reshape(-1), dev)
     mnb.mnb_gemv_gate_up_swiglu(a, wg, wu, wl.K, wl.N, wl.block_size)
-    assert mnb.mnb_last_variant() == "gemv_pair_swiglu_tma_ring"
+    assert mnb.mnb_last_variant() == "gemv_pair_swiglu_mma"
 
 
 def test_device_status_is_clean_after_the_suite(env):
