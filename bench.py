@@ -377,10 +377,30 @@ class DeviceBench:
         self.launches += steps * res["calls_per_replay"]
         us = dt * 1e6 / (steps * res["calls_per_replay"])
         wl = syn.WORKLOADS[res["workload"]]
+        # One call as a caller makes it: A in, one mnb_gemv through the binding (no graph),
+        # Y out, synchronised; host-to-host latency per call, median over the samples.
+        mnb = self.mnb
+        pk, sc, zp = res["buffers"][0]
+        single = []
+        for i in range(steps + 3):
+            t1 = time.perf_counter()
+            res["A"].copy_(A_host, non_blocking=True)
+            mnb.mnb_gemv(res["A"], pk, sc, zp, wl.K, wl.N, wl.block_size, out=res["Y"])
+            Y_host.copy_(res["Y"], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            if i >= 3:
+                single.append(time.perf_counter() - t1)
+        self.launches += steps + 3
+        us1 = float(np.median(single)) * 1e6
         return {"value": call_bytes(wl) / (us * 1e3), "unit": "GB/s", "us_per_call": us,
                 "h2d_bytes_per_step": int(A_host.numel() * 2),
                 "d2h_bytes_per_step": int(Y_host.numel() * 2),
-                "note": "pinned host A -> device, one graph replay of the 1000 calls, device Y -> pinned host, synchronised, per step"}
+                "note": "pinned host A -> device, one graph replay of the 1000 calls, device Y -> pinned host, "
+                        "synchronised, per step",
+                "single_call": {"us_host_to_host_median": us1, "samples": len(single),
+                                "note": "one eager mnb_gemv per sample with its own 8 KB copy in and 8 KB copy "
+                                        "out, synchronised: the per-call host latency (launch and copies "
+                                        "included, nothing amortised)"}}
 
 
 def log(msg: str):

@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                                c_int, vp, vp]),
         "mnb_set_programmatic_launch": (None, [c_int]),
         "mnb_check_device_status": (c_int, []),
+        "mnb_selftest_wait_timeout": (c_int, [ctypes.c_uint, vp]),
         "mnb_last_error": (ctypes.c_char_p, []),
         "mnb_last_variant": (ctypes.c_char_p, []),
         "mnb_version": (ctypes.c_char_p, []),
@@ -157,6 +158,11 @@ def mnb_set_programmatic_launch(enable: bool) -> None:
 def mnb_check_device_status() -> None:
     """Raises MnbError(MNB_ERR_TIMEOUT) if a device-side bounded wait gave up since the last check."""
     _raise(load_library().mnb_check_device_status())
+
+
+def mnb_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launches the bounded-wait self-test kernel (its wait gives up after ``limit_us``)."""
+    _raise(load_library().mnb_selftest_wait_timeout(limit_us, _stream_handle(stream)))
 
 
 def mnb_repacked_bytes(K: int, N: int, block_size: int) -> int:

@@ -152,6 +152,16 @@ mnb_status mnb_check_device_status(void) {
               "or block_group entry outside its range; that element was written as 0)", fn, v);
 }
 
+mnb_status mnb_selftest_wait_timeout(unsigned int limit_us, mnb_stream stream) {
+  const char* fn = "mnb_selftest_wait_timeout";
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(MNB_ERR_INVALID_ARG, "%s: limit_us = %u is outside 1 .. 1000000", fn, limit_us);
+  mnb::LaunchCtx ctx;
+  mnb_status st;
+  if ((st = make_ctx(fn, stream, &ctx)) != MNB_OK) return st;
+  return finish(fn, mnb::launch_wait_selftest(ctx, (uint64_t)limit_us * 1000ull), ctx);
+}
+
 mnb_status mnb_dequant(mnb_weight w, int K, int N, int block_size, float* out_kn,
                        mnb_stream stream) {
   const char* fn = "mnb_dequant";

@@ -225,6 +225,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// As mbar_wait_bounded with a caller-chosen time limit (the poll limit still applies).
+__device__ __forceinline__ bool mbar_wait_bounded_ns(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 15u && global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+
 // Spin (no suspension) on the phase: for latency-critical single threads such as the
 // MMA issuer.  Bounded like mbar_wait_bounded.
 __device__ __forceinline__ bool mbar_spin_bounded(uint64_t* bar, uint32_t parity) {

@@ -52,6 +52,8 @@ cudaError_t launch_gemv_pair_swiglu_tma(LaunchCtx& ctx, const void* A, const QWe
 cudaError_t launch_gemv_mma(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs, void* Y);
 cudaError_t launch_gemv_pair_swiglu_mma(LaunchCtx& ctx, const void* A, const QWeight& gate, const QWeight& up,
                                         int K, int N, int bs, void* out);
+// One-thread kernel whose bounded wait on a never-armed mbarrier gives up after limit_ns.
+cudaError_t launch_wait_selftest(LaunchCtx& ctx, uint64_t limit_ns);
 // Register-pipelined M = 1 GEMV; cudaErrorNotSupported when the shape has no variant.
 cudaError_t launch_gemv(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs,
                         void* Y);

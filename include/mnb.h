@@ -339,6 +339,16 @@ MNB_API void mnb_set_programmatic_launch(int enable);
  */
 MNB_API mnb_status mnb_check_device_status(void);
 
+/*
+ * Self-test of the failure path above (no counterpart on the pages; the bounded waits are
+ * this library's own): launches one kernel on `stream` whose bounded wait on a
+ * shared-memory barrier that nothing ever arrives on gives up after `limit_us`
+ * microseconds (1 .. 1000000, else MNB_ERR_INVALID_ARG), sets the wait bit of the device
+ * status word and returns. Nothing faults and the context stays usable; the next
+ * mnb_check_device_status returns MNB_ERR_TIMEOUT and clears the word. For tests.
+ */
+MNB_API mnb_status mnb_selftest_wait_timeout(unsigned int limit_us, mnb_stream stream);
+
 /* Message of the last failed call on this host thread ("" if none). */
 MNB_API const char *mnb_last_error(void);
 

@@ -1,9 +1,14 @@
-"""The act-order entry point that allocates nothing, against the workspace entry point.
+"""The act-order entry point that allocates nothing, against the oracle.
 
-mnb_gemm_act_order_noalloc keeps its scratch in a static device array inside the
-library.  Two calls in a row with different shapes (the second reads less than the
-first left behind) each match mnb_gemm_act_order within the product tolerance
-|y - y_ref| <= 2e-3 * sum_k |a_k w_nk| + 1e-5, and an oversized call is refused.
+mnb_gemm_act_order_noalloc is for callers that cannot allocate device memory: it keeps
+its scratch (the gathered activation rows, then K-slice partials) in a static device
+array inside the library instead of a caller workspace.  Calls in a row with different
+shapes -- a small-M call, then a smaller small-M call that reads scratch the first one
+left behind, then an M > 16 call on the tensor-core kernel whose K-split partials also
+live in that scratch -- each match the fp64 oracle within the product tolerance
+|y - y_ref| <= 2e-3 * sum_k |a_k w_nk| + 1e-5, element by element, and each agrees with
+the workspace entry point mnb_gemm_act_order to the same bound.  An oversized call is
+refused.
 """
 from __future__ import annotations
 
@@ -14,7 +19,7 @@ import pytest
 
 import mnb_synth as syn
 from oracle import mnb_oracle as orc
-from tests.helpers import TOL_ABS, TOL_REL, upload_act, upload_weight
+from tests.helpers import TOL_ABS, TOL_REL, assert_within_bound, upload_act, upload_weight
 
 pytestmark = pytest.mark.gpu
 
@@ -38,8 +43,8 @@ def _case(mnb, torch, dev, name, M, K, N, bs, kind):
     kp, perm, bg = mnb.mnb_act_order_plan(g_idx, K, bs)
     perm_d = torch.from_numpy(perm).to(dev)
     prep = mnb.mnb_act_order_prepare(*upload_weight(w, dev), K, N, bs, perm_d, torch.from_numpy(bg).to(dev), kp)
-    _, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs, g_idx)
-    return upload_act(A, dev), kp, perm_d, prep, B
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs, g_idx)
+    return upload_act(A, dev), kp, perm_d, prep, Y, B
 
 
 def _call_noalloc(mnb, torch, a, M, prep, perm_d, K, kp, N, bs, y, repacked_ptr=None):
@@ -53,29 +58,40 @@ def _call_noalloc(mnb, torch, a, M, prep, perm_d, K, kp, N, bs, y, repacked_ptr=
                                           ctypes.c_void_p(y.data_ptr()), stream)
 
 
-def test_noalloc_matches_workspace_entry_two_calls_in_a_row(env):
+def test_noalloc_matches_oracle_calls_in_a_row(env):
     mnb, torch, dev = env
-    cases = [("noalloc_first", 8, 2048, 384, 64, "uneven"), ("noalloc_second", 1, 1024, 200, 32, "act_order")]
+    cases = [("noalloc_first", 8, 2048, 384, 64, "act_order"),
+             ("noalloc_second", 4, 1024, 200, 32, "act_order"),
+             ("noalloc_tc", 40, 1024, 300, 64, "uneven")]
     prepared = [_case(mnb, torch, dev, *c) for c in cases]
-    outs = []
-    for (name, M, K, N, bs, _), (a, kp, perm_d, prep, B) in zip(cases, prepared):
+    # the second call gathers fewer rows than the first left in the scratch
+    assert cases[1][1] * prepared[1][1] < cases[0][1] * prepared[0][1]
+    outs, variants, reps = [], [], []
+    for (name, M, K, N, bs, _), (a, kp, perm_d, prep, Y, B) in zip(cases, prepared):
+        rep = mnb.mnb_repack(prep[0], kp, N, bs) if M > 16 else None
+        reps.append(rep)
         y = torch.full((M, N), float("nan"), dtype=torch.float16, device=dev)
-        st = _call_noalloc(mnb, torch, a, M, prep, perm_d, K, kp, N, bs, y)
+        st = _call_noalloc(mnb, torch, a, M, prep, perm_d, K, kp, N, bs, y,
+                           repacked_ptr=rep.data_ptr() if rep is not None else None)
         assert st == mnb.MNB_OK, mnb.mnb_last_error()
+        variants.append(mnb.mnb_last_variant())
         outs.append(y)
-    for (name, M, K, N, bs, _), (a, kp, perm_d, prep, B), y in zip(cases, prepared, outs):
-        ref = mnb.mnb_gemm_act_order(a, *prep, perm_d, K, kp, N, bs)
+    torch.cuda.synchronize()
+    assert variants[0].startswith("gemm_smallm") and variants[1].startswith("gemm_smallm"), variants
+    assert variants[2].startswith("gemm_tcgen05"), variants
+    for (name, M, K, N, bs, _), (a, kp, perm_d, prep, Y, B), y, rep in zip(cases, prepared, outs, reps):
+        assert_within_bound(y.double().cpu().numpy(), Y, B, name)
+        ref = mnb.mnb_gemm_act_order(a, *prep, perm_d, K, kp, N, bs, repacked=rep)
         torch.cuda.synchronize()
         got = y.double().cpu().numpy()
         want = ref.double().cpu().numpy()
-        assert np.all(np.isfinite(got)), name
         assert np.all(np.abs(got - want) <= TOL_REL * B + TOL_ABS), name
     mnb.mnb_check_device_status()
 
 
 def test_noalloc_refuses_more_than_its_scratch(env):
     mnb, torch, dev = env
-    a, kp, perm_d, prep, _ = _case(mnb, torch, dev, "noalloc_big", 1, 4096, 64, 128, "act_order")
+    a, kp, perm_d, prep, _, _ = _case(mnb, torch, dev, "noalloc_big", 1, 4096, 64, 128, "act_order")
     y = torch.empty((1, 64), dtype=torch.float16, device=dev)
     big_m = (8 << 20) // (kp * 2) + 1   # one row more than the 8 MiB scratch holds
     a_big = torch.zeros((big_m, 4096), dtype=torch.float16, device=dev)
