@@ -494,6 +494,17 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_stream_control() -> str:
+    """Compiles and runs the streaming-only control; returns its JSON line."""
+    root = os.path.dirname(os.path.abspath(__file__))
+    exe = os.path.join(root, "_build", "stream_control")
+    os.makedirs(os.path.dirname(exe), exist_ok=True)
+    src = os.path.join(root, "bench_stream_control.cu")
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-I",
+                    os.path.join(root, "gemm_mnb_gemv_gb300", "csrc"), src, "-o", exe], check=True)
+    return subprocess.run([exe], check=True, capture_output=True, text=True).stdout.strip()
+
+
 def run_single(db, name, steps, warmup):
     W = syn.WORKLOADS
     if name == "attn":
@@ -563,7 +574,13 @@ def main():
                          "with the weights], prefill, mlp_chain, "
                          "act_order_attn, f32_attn, f32_prefill) "
                          "and print its record; for profiling")
+    ap.add_argument("--stream-control", action="store_true",
+                    help="build and run bench_stream_control.cu (the M = 1 GEMV's copy and launch structure with "
+                         "no arithmetic) and print its record")
     args = ap.parse_args()
+    if args.stream_control:
+        print(run_stream_control())
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -1,51 +1,54 @@
 // M = 1 GEMV (and the paired gate/up SwiGLU GEMV) with the multiply-accumulate on the
 // tensor cores: mma.sync m16n8k16, fp16 operands, fp32 accumulate.
 //
-// Why: a decode GEMV moves ~0.58 bytes per weight, and at HBM rate a CUDA-core inner loop
-// (nibble conversion plus one mixed-precision FMA per weight) runs out of instruction
-// issue before it runs out of bandwidth.  Here the conversion is the only per-weight work:
-// the products and sums go to the tensor cores, ~1.6 issued instructions per weight
-// instead of ~3.2.
+// Why: a decode GEMV moves ~0.58 bytes per weight, and a CUDA-core inner loop (nibble
+// conversion plus one mixed-precision FMA per weight) runs out of instruction issue before
+// it runs out of bandwidth.  Here the conversion is the only per-weight CUDA-core work;
+// the products and sums go to the tensor cores.
 //
 // Data flow.  A CTA owns a contiguous range of 16-row weight tiles (rows are output
-// columns n).  A producer warp streams each tile, optionally in K slices, into a ring of
-// shared-memory stages: packed rows by one 1-D bulk copy per row at a stride of
-// (slice bytes + 16), scales as 128-byte-swizzled 2-D tensor boxes (16 rows x 128 bytes),
-// zero points as one copy of the tile's rows.  Consumer warps split each tile's K range
-// into blocks of 256 k (8 chunks of 32 k) and walk their blocks in every tile.
+// columns n).  A producer lane streams each tile into a ring of shared-memory stages, one
+// weight and one K slice per stage, with three copies: the packed bytes as one 3-D tensor
+// box (128 bytes x 16 rows x the slice's 128-byte segments), the scales as one 3-D box (or
+// one 2-D box per 128 bytes when scale rows are not whole 128 bytes), the zero points of
+// the tile's rows as one bulk copy.  Both boxes are 128-byte swizzled: 16-byte unit u of
+// row r sits at unit u ^ (r mod 8) of its 128-byte line.  Consumer warps split each
+// slice into blocks of 256 k (one packed segment, 8 chunks of 32 k).
 //
-// The MMA mapping.  Lane (g, t) (g = lane / 4, t = lane % 4) reads the two 16-byte chunks
-// 2t and 2t + 1 of a block from rows g and g + 8 and converts each 32-bit word into exact
-// fp16 (code - zp) (magic-number conversion, zero point folded into its constants).  Word
-// q of chunk 2t feeds the "X" MMAs of step q and word q of chunk 2t + 1 the "Y" MMAs, as
-// the A operand (rows g, g + 8; the k order inside an MMA is the conversion's pairing,
-// used identically for both operands).  The B operand holds the activation: column c of
-// B carries chunk c of the block at the k slots of lane c / 2 and zero elsewhere, so in
-// the X MMAs column 2t of D is row n's partial dot with chunk 2t, and in the Y MMAs column
-// 2t + 1 is its partial dot with chunk 2t + 1; the other columns are never read.  Lane
-// (g, t) therefore receives exactly the partial dots of its own chunks (D registers 0 and
-// 2 of X, 1 and 3 of Y) and multiplies each by the scale of its group (scale after the
-// partial dot of each 32-element chunk, as the fp16 GEMV of matmul_nbits.rs applies its
-// per-block scale), accumulating in fp32.  Only 8 lanes of a warp load B; the other lanes
-// keep zero registers.
+// The MMA mapping.  Lane (g, t) (g = lane / 4, t = lane % 4) reads chunks 2t and 2t + 1 of
+// a block from rows g and g + 8 and converts each 32-bit word into exact fp16 (code - zp)
+// (magic-number conversion, zero point folded into its constants).  Word q of chunk 2t
+// feeds the "X" MMAs of step q and word q of chunk 2t + 1 the "Y" MMAs, as the A operand
+// (rows g, g + 8; the k order inside an MMA is the conversion's pairing, used identically
+// for both operands).  The B operand holds the activation: column c of B carries chunk c
+// of the block at the k slots of lane c / 2 and zero elsewhere, so in the X MMAs column 2t
+// of D is row n's partial dot with chunk 2t, and in the Y MMAs column 2t + 1 is its partial
+// dot with chunk 2t + 1; the other columns are never read.  Lane (g, t) therefore receives
+// exactly the partial dots of its own chunks (D registers 0 and 2 of X, 1 and 3 of Y) and
+// multiplies each by the scale of its group (scale after the partial dot of each
+// 32-element chunk, as the fp16 GEMV of matmul_nbits.rs applies its per-block scale),
+// accumulating in fp32.  Only 8 lanes of a warp load B; the other lanes keep zeros.
 //
-// Bank conflicts.  Packed rows sit at a stride of 16 mod 128 bytes, so the 8 lanes of a
-// quarter-warp (rows g, g + 1, chunks 2t or 2t + 1) read 8 different 16-byte units.  Scale
-// boxes are swizzled (unit u of row r at u ^ (r mod 8)), so rows 0..7 read distinct banks.
+// Bank conflicts.  In a swizzled segment the 8 lanes of a quarter-warp (rows g, g + 1,
+// chunk 2t or 2t + 1) read 8 different 16-byte units; rows g and g + 8 share a swizzle.
 // The activation is staged once per CTA (after the programmatic-launch wait; each warp
 // stages only the blocks it uses, so no CTA-wide barrier) in MMA order: block kb, step q,
 // chunk c at byte (kb * 32 + q * 8 + c) * 16, the 8 halves paired as the conversion pairs
 // nibbles.
 //
-// Launch overlap.  When a CTA's whole share of the weights fits in half an SM's shared
-// memory, the kernel runs 8 consumer warps with at most half the registers, so the next
-// call's CTA can be resident on the same SM: its producer streams all of its stages before
-// the programmatic-launch wait, while this call computes.  Larger problems run one CTA per
-// SM with 16 consumer warps and a deeper ring.
+// Tile sums.  After a tile each warp sums its four lanes per row and posts the partials of
+// its 16 rows; the last warp to post (a shared-memory counter) adds them in warp order and
+// stores the tile, so no warp waits on the others.
+//
+// Launch overlap.  When a CTA's whole share fits half an SM (8 consumer warps, at most half
+// the SM's registers and shared memory each), one CTA per SM per call: the next call's CTA
+// is resident while this call runs and its producer streams all of its stages before the
+// programmatic-launch wait.  Larger problems run two CTAs of the same call per SM when
+// stages of at least 32 KB fit half an SM, else one CTA per SM with 16 consumer warps and
+// a deeper ring.
 //
 // Every wait is bounded; a wait that gives up records its cause in the device status word
-// and the affected tile's outputs are NaN.  Each tile's sum over warps is taken in warp
-// order after a consumer barrier, so results are deterministic.
+// and the affected tile's outputs are NaN.  Results are deterministic.
 #include <cuda.h>
 #include <cstring>
 #include <cudaTypedefs.h>
@@ -58,30 +61,27 @@
 namespace mnb {
 namespace {
 
-constexpr int kRows = 16;     // weight rows per tile (the MMA's M)
-constexpr int kBlockK = 256;  // k per block (8 chunks of 32)
-constexpr int kRowPad = 16;   // staged packed row stride = slice bytes + 16
+constexpr int kRows = 16;        // weight rows per tile (the MMA's M)
+constexpr int kBlockK = 256;     // k per block (8 chunks of 32): one 128-byte packed segment
 constexpr int kMaxStages = 8;
-constexpr int kBoxBytes = 2048;  // one scale box: 16 rows x 128 bytes
+constexpr int kBoxBytes = 2048;  // one swizzled box slab: 16 rows x 128 bytes
 
 struct MmaGemvArgs {
   const __half* A;
-  const uint8_t* packed[2];
   const uint8_t* zp[2];
   void* Y;
   int K, N;
-  int gshift;        // log2(bs / 32)
-  int row_bytes;     // K / 2
   int kslice, nslices;
-  int prow;          // kslice / 2 + kRowPad
-  int sslice;        // scale bytes per row of a (full) slice
+  int nseg;          // 128-byte packed segments (256 k) per row of a full slice
+  int sslice;        // scale bytes per row of a full slice
+  int s3d;           // scales copied as one 3-D box per stage (scale rows in whole 128 bytes)
+  int nsbox;         // scale boxes (16 rows x 128 bytes) per stage
   int zrow;          // zero-point bytes per row (0: none); whole-K stages only
-  int poff, zoff;    // packed rows and zero points inside a weight's sub-stage
-  int wbytes;        // one weight's sub-stage (multiple of 1024)
-  int stage_bytes;   // NWT * wbytes
+  int poff, zoff;    // packed segments and zero points inside a stage
+  int stage_bytes;   // one stage: one weight's tile slice (multiple of 1024)
   int stages;
+  int red_off;       // tile-sum slots after the activation: [stages + 1][weights][warps][16]
   int ntiles;
-  int ssz;           // bytes per scale
   uint32_t* status;
   const __half* bias;
   int bias_mode;
@@ -104,38 +104,38 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int q) {
   return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
 }
 
-// Shared address of byte o of row r in a weight sub-stage's swizzled scale boxes.
-__device__ __forceinline__ uint32_t scale_addr(uint32_t wbase, int r, int o) {
-  return wbase + (uint32_t)((o >> 7) * kBoxBytes + r * 128 + ((((o & 127) >> 4) ^ (r & 7)) << 4) + (o & 15));
-}
-
-// The two scales (chunks 2t and 2t + 1 of a block) of row r, as fp32.
+// The two scales (chunks 2t and 2t + 1 of a block) at shared address `addr`, as fp32: for
+// block size 32 two consecutive groups, otherwise one group.
 template <bool S16, int CPG>
-__device__ __forceinline__ void load_scales(uint32_t wbase, int r, int o0, float& s0, float& s1) {
+__device__ __forceinline__ void load_scales(uint32_t addr, float& s0, float& s1) {
   if constexpr (CPG == 1) {
     if constexpr (S16) {
-      const uint32_t h = lds_u32_a(scale_addr(wbase, r, o0));
+      const uint32_t h = lds_u32_a(addr);
       s0 = half_bits_to_float(h & 0xffffu);
       s1 = half_bits_to_float(h >> 16);
     } else {
-      const uint2 f = lds_u64_a(scale_addr(wbase, r, o0));
+      const uint2 f = lds_u64_a(addr);
       s0 = __uint_as_float(f.x);
       s1 = __uint_as_float(f.y);
     }
   } else {
-    s0 = S16 ? half_bits_to_float(lds_u16_a(scale_addr(wbase, r, o0))) : __uint_as_float(lds_u32_a(scale_addr(wbase, r, o0)));
+    s0 = S16 ? half_bits_to_float(lds_u16_a(addr)) : __uint_as_float(lds_u32_a(addr));
     s1 = s0;
   }
 }
 
-template <int NCW, bool PAIR, bool S16, bool ZP, int CPG>
-__global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
-    gemv_mma_kernel(const MmaGemvArgs p, const __grid_constant__ CUtensorMap tmap0,
-                    const __grid_constant__ CUtensorMap tmap1) {
+// CPG: 32-k chunks per quant group (1, 2, 4 for block sizes 32, 64, 128).  TWO: two CTAs
+// share an SM (launch bounds that leave each at most half the registers).
+template <int NCW, bool TWO, bool PAIR, bool S16, bool ZP, int CPG>
+__global__ void __launch_bounds__((NCW + 1) * 32, TWO ? 2 : 1)
+    gemv_mma_kernel(const MmaGemvArgs p, const __grid_constant__ CUtensorMap tmp0,
+                    const __grid_constant__ CUtensorMap tmp1, const __grid_constant__ CUtensorMap tms0,
+                    const __grid_constant__ CUtensorMap tms1) {
   constexpr int NWT = PAIR ? 2 : 1;
+  constexpr int kSsz = S16 ? 2 : 4;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
-  __shared__ float red[2][NWT][NCW][kRows];
+  __shared__ unsigned red_cnt[kMaxStages + 1];
   __shared__ int failed;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -143,9 +143,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned (swizzled boxes)
   const uint32_t ring_u32 = smem_u32(ring);
   const uint32_t act_u32 = ring_u32 + (uint32_t)(p.stages * p.stage_bytes);
+  float* red = reinterpret_cast<float*>(ring + p.red_off);
   const int t_begin = (int)(((long long)blockIdx.x * p.ntiles) / gridDim.x);
   const int t_end = (int)(((long long)(blockIdx.x + 1) * p.ntiles) / gridDim.x);
-  const int nst = (t_end - t_begin) * p.nslices;
+  const int nsub = NWT * p.nslices;  // stages per tile: weight-major, then K slice
+  const int nst = (t_end - t_begin) * nsub;
   const int S = p.stages;
   const int bps = p.kslice / kBlockK;  // blocks in a full slice
 
@@ -155,61 +157,67 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], NCW);
     }
+    for (int s = 0; s <= S; ++s) red_cnt[s] = 0u;
     fence_mbar_init();
   }
   __syncthreads();
 
   if (warp == NCW) {
     // ------------------------------- producer -------------------------------------
-    int slot = 0, issued = 0;
-    uint32_t phase = 0;
-    for (int st = 0; st < nst; ++st) {
-      int free_slot = 1;
-      if (lane == 0 && st >= S && !mbar_wait_bounded(&empty_bar[slot], phase ^ 1u)) {
-        report_status(p.status, kStatusEmptyWait);
-        atomicExch(&failed, 1);
-        free_slot = 0;
+    if (lane == 0) {
+      int slot = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int st = 0; st < nst; ++st) {
+        if (st >= S && !mbar_wait_bounded(&empty_bar[slot], phase ^ 1u)) {
+          report_status(p.status, kStatusEmptyWait);
+          atomicExch(&failed, 1);
+          break;
+        }
+        const int r = st % nsub;
+        const int ti = t_begin + st / nsub, wt = r / p.nslices, si = r % p.nslices;
+        const int n0 = ti * kRows, nr = min(kRows, p.N - n0);
+        const int klen = min(p.kslice, p.K - si * p.kslice);
+        const int nsb = p.s3d ? p.nsbox : (((klen / (32 * CPG)) * kSsz + 127) >> 7);
+        const uint32_t bytes = (uint32_t)((p.nseg + nsb) * kBoxBytes) + (uint32_t)(ZP ? nr * p.zrow : 0);
+        const bool w1 = NWT == 2 && wt == 1;
+        uint8_t* wb = ring + (size_t)slot * p.stage_bytes;
+        mbar_arrive_expect_tx(&full_bar[slot], bytes);
+        // rows past N and segments past K arrive as zeros (and count in full)
+        tc::tma_load_3d(wb + p.poff, w1 ? &tmp1 : &tmp0, 0, n0, si * bps, &full_bar[slot]);
+        if (p.s3d)
+          tc::tma_load_3d(wb, w1 ? &tms1 : &tms0, 0, n0, (si * p.sslice) >> 7, &full_bar[slot]);
+        else
+          for (int b = 0; b < nsb; ++b)
+            tc::tma_load_2d(wb + b * kBoxBytes, w1 ? &tms1 : &tms0, si * p.sslice + b * 128, n0, &full_bar[slot]);
+        if (ZP)
+          bulk_g2s(wb + p.zoff, (w1 ? p.zp[1] : p.zp[0]) + (long long)n0 * p.zrow, (uint32_t)(nr * p.zrow),
+                   &full_bar[slot]);
+        issued = st + 1;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
-      if (!__shfl_sync(kFull, free_slot, 0)) break;
-      const int ti = t_begin + st / p.nslices, si = st % p.nslices;
-      const int n0 = ti * kRows, nr = min(kRows, p.N - n0);
-      const int k0 = si * p.kslice, klen = min(p.kslice, p.K - k0);
-      const int pbytes = klen >> 1;
-      const int sb_slice = (klen >> (5 + p.gshift)) * p.ssz;  // scale bytes of this slice
-      const int nsb = (sb_slice + 127) >> 7;
-      const uint32_t bytes = (uint32_t)NWT * ((uint32_t)(nr * pbytes) + (uint32_t)(nsb * kBoxBytes) +
-                                              (uint32_t)(ZP ? nr * p.zrow : 0));
-      if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], bytes);
-      __syncwarp();
-      uint8_t* stg = ring + (size_t)slot * p.stage_bytes;
-#pragma unroll
-      for (int wt = 0; wt < NWT; ++wt) {
-        uint8_t* wb = stg + wt * p.wbytes;
-        if (lane < nr)
-          bulk_g2s(wb + p.poff + lane * p.prow, p.packed[wt] + (long long)(n0 + lane) * p.row_bytes + (k0 >> 1),
-                   (uint32_t)pbytes, &full_bar[slot]);
-        const CUtensorMap* tm = wt == 0 ? &tmap0 : &tmap1;
-        for (int b = lane - 16; b >= 0 && b < nsb; b += 16)
-          tc::tma_load_2d(wb + b * kBoxBytes, tm, si * p.sslice + b * 128, n0, &full_bar[slot]);
-        if (ZP && lane == 0)
-          bulk_g2s(wb + p.zoff, p.zp[wt] + (long long)n0 * p.zrow, (uint32_t)(nr * p.zrow), &full_bar[slot]);
-      }
-      issued = st + 1;
-      if (++slot == S) {
-        slot = 0;
-        phase ^= 1u;
-      }
-    }
-    // Every copy issued must land before the CTA exits; after a failed wait this bounds it.
-    if (lane == 0)
+      // Every copy issued must land before the CTA exits; after a failed wait this bounds it.
       for (int st = issued > S ? issued - S : 0; st < issued; ++st)
         (void)mbar_wait_bounded(&full_bar[st % S], (uint32_t)(st / S) & 1u);
+    }
+    __syncwarp();
     pdl_launch_dependents();
   } else {
     // ------------------------------- consumers ------------------------------------
     pdl_launch_dependents();
     const int g = lane >> 2, t = lane & 3;
     const uint32_t bdata = (uint32_t)((g >> 1) == t);  // this lane carries B column g
+    // Per-lane group geometry of chunks 2t and 2t + 1 of block b (compile-time block size):
+    // zero-point byte zb0 + zbs * b with the nibbles at shifts zsh0, zsh1; scale byte
+    // so0 + sos * b within the slice's scale boxes.
+    const int zb0 = CPG == 1 ? t : (CPG == 2 ? (t >> 1) : 0);
+    const int zbs = CPG == 1 ? 4 : (CPG == 2 ? 2 : 1);
+    const uint32_t zsh0 = CPG == 1 ? 0u : (CPG == 2 ? 4u * (uint32_t)(t & 1) : 4u * (uint32_t)((t >> 1) & 1));
+    const uint32_t zsh1 = CPG == 1 ? 4u : zsh0;
+    const int so0 = (CPG == 1 ? 2 * t : (CPG == 2 ? t : (t >> 1))) * kSsz;
+    const int sos = (CPG == 1 ? 8 : (CPG == 2 ? 4 : 2)) * kSsz;
     pdl_wait();
     // Stage this warp's activation blocks in MMA order (lane l holds halves 8l .. 8l + 7 of
     // a block: chunk l / 4, step l % 4).
@@ -241,89 +249,136 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
     __syncwarp();
 
     const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
-    uint32_t bq[4][4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) bq[q][0] = bq[q][1] = bq[q][2] = bq[q][3] = 0u;
     float acc[NWT][2];
     bool ok = true;
     int slot = 0;
     uint32_t phase = 0;
     for (int st = 0; st < nst; ++st) {
-      const int tl = st / p.nslices, si = st % p.nslices;
-      if (si == 0) {
+      const int tl = st / nsub, r = st % nsub;
+      const int wt = r / p.nslices, si = r % p.nslices;
+      if (r == 0) {
 #pragma unroll
-        for (int wt = 0; wt < NWT; ++wt) acc[wt][0] = acc[wt][1] = 0.0f;
+        for (int w = 0; w < NWT; ++w) acc[w][0] = acc[w][1] = 0.0f;
       }
       if (ok && !mbar_wait_bounded(&full_bar[slot], phase)) {
         report_status(p.status, kStatusFullWait);
         atomicExch(&failed, 1);
         ok = false;
       }
-      const uint32_t sb = ring_u32 + (uint32_t)(slot * p.stage_bytes);
+      const uint32_t wbase = ring_u32 + (uint32_t)(slot * p.stage_bytes);
       const int nb = (min(p.kslice, p.K - si * p.kslice)) / kBlockK;
       const int b_lo = (warp * nb) / NCW, b_hi = ok ? ((warp + 1) * nb) / NCW : b_lo;
+      float vg = 0.0f, v8 = 0.0f;  // this stage's partial sums of rows g and g + 8
       for (int b = b_lo; b < b_hi; ++b) {
-        const int kb = si * bps + b;
-        const uint32_t abase = act_u32 + (uint32_t)(kb * 512 + g * 16);
+        const uint32_t abase = act_u32 + (uint32_t)((si * bps + b) * 512 + g * 16);
+        const int o0 = so0 + sos * b;  // scale byte within the slice's boxes
+        const uint32_t soff = (uint32_t)((o0 >> 7) * kBoxBytes + g * 128 + ((((o0 & 127) >> 4) ^ g) << 4) + (o0 & 15));
+        // segment b, row g, 16-byte units 2t (X) and 2t + 1 (Y) swizzled by the row; row g + 8
+        // 1024 bytes on, same swizzle
+        const uint32_t seg = wbase + (uint32_t)(p.poff + b * kBoxBytes + g * 128);
+        const uint32_t rxa = seg + (uint32_t)(((2 * t) ^ g) << 4), rya = seg + (uint32_t)(((2 * t + 1) ^ g) << 4);
+        uint32_t bq[4][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) lds128_pred(bq[q], abase + (uint32_t)(q * 128), bdata);
-        // groups (within the slice) of chunks 2t and 2t + 1, and the scale byte offset
-        const int c0 = 8 * b + 2 * t;
-        const int gs0 = c0 >> p.gshift;
-        const int o0 = gs0 * p.ssz;
+        for (int q = 0; q < 4; ++q) {
+          bq[q][0] = bq[q][1] = bq[q][2] = bq[q][3] = 0u;
+          lds128_pred(bq[q], abase + (uint32_t)(q * 128), bdata);
+        }
+        const uint4 xa = lds128_a(rxa), ya = lds128_a(rya);
+        const uint4 xb = lds128_a(rxa + 1024u), yb = lds128_a(rya + 1024u);
+        float sa0, sa1, sb0, sb1;
+        load_scales<S16, CPG>(wbase + soff, sa0, sa1);
+        load_scales<S16, CPG>(wbase + soff + 1024u, sb0, sb1);  // row g + 8: same swizzle
+        uint32_t zlxa = zl8, zhxa = zh8, zlya = zl8, zhya = zh8;
+        uint32_t zlxb = zl8, zhxb = zh8, zlyb = zl8, zhyb = zh8;
+        if constexpr (ZP) {
+          const uint32_t zaddr = wbase + (uint32_t)(p.zoff + g * p.zrow + zb0 + zbs * b);
+          const uint32_t za = lds_u8_a(zaddr), zb = lds_u8_a(zaddr + (uint32_t)(8 * p.zrow));
+          const uint32_t za0 = (za >> zsh0) & 15u, za1 = (za >> zsh1) & 15u;
+          const uint32_t zb0v = (zb >> zsh0) & 15u, zb1v = (zb >> zsh1) & 15u;
+          zlxa = zp_lo_const(za0);
+          zhxa = zp_hi_const(za0);
+          zlya = zp_lo_const(za1);
+          zhya = zp_hi_const(za1);
+          zlxb = zp_lo_const(zb0v);
+          zhxb = zp_hi_const(zb0v);
+          zlyb = zp_lo_const(zb1v);
+          zhyb = zp_hi_const(zb1v);
+        }
+        float dx0[4], dx1[4], dy0[4], dy1[4];
 #pragma unroll
-        for (int wt = 0; wt < NWT; ++wt) {
-          const uint32_t wbase = sb + (uint32_t)(wt * p.wbytes);
-          const uint32_t ra = wbase + (uint32_t)(p.poff + g * p.prow + b * 128 + 32 * t);
-          const uint32_t rb = ra + (uint32_t)(8 * p.prow);
-          const uint4 xa = lds128_a(ra), ya = lds128_a(ra + 16u);
-          const uint4 xb = lds128_a(rb), yb = lds128_a(rb + 16u);
-          uint32_t zlxa = zl8, zhxa = zh8, zlya = zl8, zhya = zh8;
-          uint32_t zlxb = zl8, zhxb = zh8, zlyb = zl8, zhyb = zh8;
-          if constexpr (ZP) {
-            const int gs1 = (c0 + 1) >> p.gshift;
-            const uint32_t za = lds_u8_a(wbase + (uint32_t)(p.zoff + g * p.zrow + (gs0 >> 1)));
-            const uint32_t zb = lds_u8_a(wbase + (uint32_t)(p.zoff + (g + 8) * p.zrow + (gs0 >> 1)));
-            const uint32_t sh0 = (uint32_t)(gs0 & 1) * 4u, sh1 = (uint32_t)(gs1 & 1) * 4u;
-            const uint32_t za0 = (za >> sh0) & 15u, za1 = (za >> sh1) & 15u;
-            const uint32_t zb0 = (zb >> sh0) & 15u, zb1 = (zb >> sh1) & 15u;
-            zlxa = zp_lo_const(za0);
-            zhxa = zp_hi_const(za0);
-            zlya = zp_lo_const(za1);
-            zhya = zp_hi_const(za1);
-            zlxb = zp_lo_const(zb0);
-            zhxb = zp_hi_const(zb0);
-            zlyb = zp_lo_const(zb1);
-            zhyb = zp_hi_const(zb1);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t da[4], db[4], ea[4], eb[4];
+          nibbles_to_centered_half2(word_of(xa, q), zlxa, zhxa, da);
+          nibbles_to_centered_half2(word_of(xb, q), zlxb, zhxb, db);
+          nibbles_to_centered_half2(word_of(ya, q), zlya, zhya, ea);
+          nibbles_to_centered_half2(word_of(yb, q), zlyb, zhyb, eb);
+          if (q == 0) {
+            mma16816_zero(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
+            mma16816_zero(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
+            mma16816_zero(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
+            mma16816_zero(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
+          } else {
+            mma16816(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
+            mma16816(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
+            mma16816(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
+            mma16816(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
           }
-          float dx0[4], dx1[4], dy0[4], dy1[4];
+        }
+        // lane (g, t): X column 2t (registers 0, 2) and Y column 2t + 1 (registers 1, 3)
+        vg = fmaf(dx0[0] + dx1[0], sa0, vg);
+        vg = fmaf(dy0[1] + dy1[1], sa1, vg);
+        v8 = fmaf(dx0[2] + dx1[2], sb0, v8);
+        v8 = fmaf(dy0[3] + dy1[3], sb1, v8);
+      }
+      if (NWT == 1 || wt == 0) {
+        acc[0][0] += vg;
+        acc[0][1] += v8;
+      } else {
+        acc[NWT - 1][0] += vg;
+        acc[NWT - 1][1] += v8;
+      }
+      if (r == nsub - 1) {
+        // The tile is done: sum the four lanes of each row and post this warp's partials;
+        // the last warp to post adds the warps' partials in warp order and stores the tile.
+        // Slots are reused every S + 1 tiles; the slot of this stage is released only after
+        // this, so no warp can be S + 1 tiles ahead of the warp that reads a slot.
+        const int rs = tl % (S + 1);
+        float* rp = red + (size_t)rs * (NWT * NCW * kRows);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t da[4], db[4], ea[4], eb[4];
-            nibbles_to_centered_half2(word_of(xa, q), zlxa, zhxa, da);
-            nibbles_to_centered_half2(word_of(xb, q), zlxb, zhxb, db);
-            nibbles_to_centered_half2(word_of(ya, q), zlya, zhya, ea);
-            nibbles_to_centered_half2(word_of(yb, q), zlyb, zhyb, eb);
-            if (q == 0) {
-              mma16816_zero(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
-              mma16816_zero(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
-              mma16816_zero(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
-              mma16816_zero(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
-            } else {
-              mma16816(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
-              mma16816(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
-              mma16816(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
-              mma16816(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
+        for (int w = 0; w < NWT; ++w) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float x = acc[w][h];
+            x += __shfl_xor_sync(kFull, x, 1);
+            x += __shfl_xor_sync(kFull, x, 2);
+            if (t == 0) rp[(w * NCW + warp) * kRows + g + 8 * h] = x;
+          }
+        }
+        __syncwarp();
+        unsigned last = 0;
+        if (lane == 0) {
+          __threadfence_block();
+          last = atomicInc(&red_cnt[rs], (unsigned)(NCW - 1)) == (unsigned)(NCW - 1);  // wraps to 0
+        }
+        last = __shfl_sync(kFull, last, 0);
+        if (last) {
+          __threadfence_block();
+          const int n = (t_begin + tl) * kRows + lane;
+          if (lane < kRows && n < p.N) {
+            float v[NWT];
+#pragma unroll
+            for (int w = 0; w < NWT; ++w) {
+              float sum = 0.0f;
+#pragma unroll
+              for (int ww = 0; ww < NCW; ++ww) sum += *(volatile float*)&rp[(w * NCW + ww) * kRows + lane];
+              v[w] = sum;
             }
+            __half out;
+            if constexpr (PAIR) out = __float2half_rn(silu_f32(v[0]) * v[1]);
+            else out = round_out(v[0], p.bias, n, p.bias_mode);
+            if (*(volatile int*)&failed) out = __ushort_as_half(0x7e00);
+            reinterpret_cast<__half*>(p.Y)[n] = out;
           }
-          float sa0, sa1, sb0, sb1;
-          load_scales<S16, CPG>(wbase, g, o0, sa0, sa1);
-          load_scales<S16, CPG>(wbase, g + 8, o0, sb0, sb1);
-          // lane (g, t): X column 2t (registers 0, 2) and Y column 2t + 1 (registers 1, 3)
-          acc[wt][0] = fmaf(dx0[0] + dx1[0], sa0, acc[wt][0]);
-          acc[wt][0] = fmaf(dy0[1] + dy1[1], sa1, acc[wt][0]);
-          acc[wt][1] = fmaf(dx0[2] + dx1[2], sb0, acc[wt][1]);
-          acc[wt][1] = fmaf(dy0[3] + dy1[3], sb1, acc[wt][1]);
         }
       }
       __syncwarp();
@@ -332,39 +387,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
         slot = 0;
         phase ^= 1u;
       }
-      if (si == p.nslices - 1) {
-        // The tile is done: sum the four lanes of each row, then across warps in order.
-        const int buf = tl & 1;
-#pragma unroll
-        for (int wt = 0; wt < NWT; ++wt) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v = acc[wt][h];
-            v += __shfl_xor_sync(kFull, v, 1);
-            v += __shfl_xor_sync(kFull, v, 2);
-            if (t == 0) red[buf][wt][warp][g + 8 * h] = v;
-          }
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
-        if (warp == tl % NCW && lane < kRows) {
-          const int n = (t_begin + tl) * kRows + lane;
-          if (n < p.N) {
-            float v[NWT];
-#pragma unroll
-            for (int wt = 0; wt < NWT; ++wt) {
-              float s = 0.0f;
-#pragma unroll
-              for (int w = 0; w < NCW; ++w) s += red[buf][wt][w][lane];
-              v[wt] = s;
-            }
-            __half out;
-            if constexpr (PAIR) out = __float2half_rn(silu_f32(v[0]) * v[1]);
-            else out = round_out(v[0], p.bias, n, p.bias_mode);
-            if (failed) out = __ushort_as_half(0x7e00);
-            reinterpret_cast<__half*>(p.Y)[n] = out;
-          }
-        }
-      }
     }
   }
 }
@@ -372,26 +394,34 @@ __global__ void __launch_bounds__((NCW + 1) * 32, (NCW <= 8 ? 2 : 1))
 // ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
-using MmaKernel = void (*)(const MmaGemvArgs, const CUtensorMap, const CUtensorMap);
+using MmaKernel = void (*)(const MmaGemvArgs, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                           const CUtensorMap);
 
-template <int NCW, bool PAIR, bool S16, bool ZP>
+// Consumer warps: 8 when two CTAs share an SM (at most half its registers each), else 16.
+constexpr int kNcwTwo = 8, kNcwOne = 16;
+
+template <bool TWO, bool PAIR, bool S16, bool ZP>
 MmaKernel pick_cpg(int cpg) {
-  if (cpg == 1) return gemv_mma_kernel<NCW, PAIR, S16, ZP, 1>;
-  if (cpg == 2) return gemv_mma_kernel<NCW, PAIR, S16, ZP, 2>;
-  if (cpg == 4) return gemv_mma_kernel<NCW, PAIR, S16, ZP, 4>;
+  constexpr int NCW = TWO ? kNcwTwo : kNcwOne;
+  if (cpg == 1) return gemv_mma_kernel<NCW, TWO, PAIR, S16, ZP, 1>;
+  if (cpg == 2) return gemv_mma_kernel<NCW, TWO, PAIR, S16, ZP, 2>;
+  if (cpg == 4) return gemv_mma_kernel<NCW, TWO, PAIR, S16, ZP, 4>;
   return nullptr;
 }
 
-template <int NCW, bool PAIR>
+template <bool TWO, bool PAIR>
 MmaKernel pick(bool s16, bool zp, int cpg) {
-  if (s16) return zp ? pick_cpg<NCW, PAIR, true, true>(cpg) : pick_cpg<NCW, PAIR, true, false>(cpg);
-  return zp ? pick_cpg<NCW, PAIR, false, true>(cpg) : pick_cpg<NCW, PAIR, false, false>(cpg);
+  if (s16) return zp ? pick_cpg<TWO, PAIR, true, true>(cpg) : pick_cpg<TWO, PAIR, true, false>(cpg);
+  return zp ? pick_cpg<TWO, PAIR, false, true>(cpg) : pick_cpg<TWO, PAIR, false, false>(cpg);
 }
 
-// Dynamic shared memory per CTA when two CTAs share an SM (the calls overlap), and when one
-// CTA has the SM.
-constexpr int kHalfSmBudget = 100 * 1024;
-constexpr int kFullSmBudget = 200 * 1024;
+// Dynamic shared memory per CTA when two CTAs share an SM, and when one CTA has the SM; the
+// stage size aimed at (several stages in flight per CTA).
+constexpr int kTwoBudget = 100 * 1024;
+constexpr int kOneBudget = 200 * 1024;
+constexpr int kStageTargetTwo = 40 * 1024;
+constexpr int kStageTargetOne = 72 * 1024;
+constexpr int kTwoMinStage = 32 * 1024;
 
 template <bool PAIR>
 cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int K, int N, int bs, void* Y) {
@@ -412,86 +442,126 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   a.Y = Y;
   a.K = K;
   a.N = N;
-  a.gshift = bs == 32 ? 0 : (bs == 64 ? 1 : 2);
-  a.row_bytes = K / 2;
-  a.ssz = ssz;
   a.zrow = zp ? (G + 1) / 2 : 0;
   a.ntiles = (N + kRows - 1) / kRows;
   // A partial last tile copies nr * zrow zero-point bytes: a 16-byte multiple is required.
   if (zp && ((N % kRows) * a.zrow) % 16 != 0) return cudaErrorNotSupported;
-  for (int t = 0; t < 2; ++t) {
-    const QWeight& q = w[t < NWT ? t : 0];
-    a.packed[t] = q.packed;
-    a.zp[t] = q.zp;
-  }
+  for (int t = 0; t < 2; ++t) a.zp[t] = w[t < NWT ? t : 0].zp;
   const int act_bytes = K * 2;
-  // Sub-stage layout for a K slice of ks: [scale boxes][packed rows][zero points], 1024-aligned.
+  // Stage layout for a K slice of ks: [scale boxes][packed segments][zero points], 1024-aligned.
   auto layout = [&](int ks) {
     a.kslice = ks;
     a.nslices = (K + ks - 1) / ks;
-    a.prow = ks / 2 + kRowPad;
+    a.nseg = ks / kBlockK;
     a.sslice = (ks / bs) * ssz;
-    const int nsb = (a.sslice + 127) / 128;
-    a.poff = nsb * kBoxBytes;
-    a.zoff = a.poff + kRows * a.prow;
-    a.wbytes = (a.zoff + kRows * a.zrow + 1023) / 1024 * 1024;
-    a.stage_bytes = NWT * a.wbytes;
+    a.nsbox = (a.sslice + 127) / 128;
+    a.poff = a.nsbox * kBoxBytes;
+    a.zoff = a.poff + a.nseg * kBoxBytes;
+    a.stage_bytes = (a.zoff + kRows * a.zrow + 1023) / 1024 * 1024;
   };
-  int grid = ctx.num_sms < a.ntiles ? ctx.num_sms : a.ntiles;
-  const int max_tiles = (a.ntiles + grid - 1) / grid;
-  // Two CTAs per SM when every stage of a CTA fits half the SM: all of its weights are then
-  // requested at once, before the programmatic-launch wait.
-  layout(K);
-  bool half_sm = (size_t)max_tiles * a.stage_bytes + act_bytes + 1024 <= (size_t)kHalfSmBudget;
-  if (half_sm) {
-    a.stages = max_tiles;
-  } else {
-    // One CTA per SM: the whole K range per stage when two stages fit, else K slices (whole
-    // 256-k blocks, scale bytes in whole boxes; no zero points).
-    int ks = K;
-    auto fits = [&]() { return 2 * (size_t)a.stage_bytes + act_bytes + 1024 <= (size_t)kFullSmBudget; };
-    if (!fits()) {
-      ks = 0;
-      if (zp) return cudaErrorNotSupported;
-      for (int cand = (K / 2) / kBlockK * kBlockK; cand >= 1024; cand -= kBlockK) {
-        if (cand % bs != 0 || ((cand / bs) * ssz) % 128 != 0) continue;
-        layout(cand);
-        if (fits()) {
-          ks = cand;
-          break;
-        }
-      }
-      if (ks == 0) return cudaErrorNotSupported;
+  // The K slice: the whole K range when its stage is at most `target`, else the largest
+  // slice (whole 256-k blocks and quant groups, scale bytes in whole 128 bytes; not with
+  // zero points) that is, else the smallest such slice.  False if there is none.
+  auto choose = [&](int target) {
+    layout(K);
+    if (a.stage_bytes <= target || zp) return true;  // zero points: whole-K stages only
+    int smallest = 0;
+    for (int cand = (K - 1) / kBlockK * kBlockK; cand >= kBlockK; cand -= kBlockK) {
+      if (cand % bs != 0 || ((cand / bs) * ssz) % 128 != 0) continue;
+      smallest = cand;
+      layout(cand);
+      if (a.stage_bytes <= target) return true;
     }
-    a.stages = (int)((kFullSmBudget - act_bytes - 1024) / a.stage_bytes);
-    if (a.stages > kMaxStages) a.stages = kMaxStages;
+    if (smallest == 0) return false;
+    layout(smallest);
+    return true;
+  };
+  // Launch shape, in order of preference:
+  //  * two CTAs per SM, one CTA per SM per call, when all of a CTA's stages fit half an SM:
+  //    every weight byte is requested at once and the next call's CTA streams its weights
+  //    while this call computes;
+  //  * two CTAs of the same call per SM when stages of at least kTwoMinStage fit half an SM
+  //    (two stages in flight per CTA, sixteen warps computing per SM);
+  //  * else one CTA per SM with sixteen consumer warps and a deeper ring.
+  // each stage also needs one tile-sum slot (plus one spare slot)
+  const int rps_two = NWT * kNcwTwo * kRows * 4, rps_one = NWT * kNcwOne * kRows * 4;
+  const int avail = kTwoBudget - act_bytes - rps_two - 1024;
+  int grid = 0;
+  bool two = false;
+  for (int mult = 1; mult <= 2 && !two; ++mult) {
+    const int g = ctx.num_sms * mult < a.ntiles ? ctx.num_sms * mult : a.ntiles;
+    const int max_tiles = (a.ntiles + g - 1) / g;
+    for (int want = 3; want >= 2 && !two && avail > 0; --want) {
+      const int target = avail / want - rps_two < kStageTargetTwo ? avail / want - rps_two : kStageTargetTwo;
+      if (!choose(target)) continue;
+      const int need = max_tiles * NWT * a.nslices;  // stages of the busiest CTA
+      int stages = avail / (a.stage_bytes + rps_two);
+      if (stages > kMaxStages) stages = kMaxStages;
+      if (stages > need) stages = need;
+      const bool all_fit = stages >= 1 && stages == need;
+      if ((mult == 1 && all_fit) || (mult == 2 && stages >= 2 && a.stage_bytes >= kTwoMinStage)) {
+        two = true;
+        grid = g;
+        a.stages = stages;
+      }
+    }
   }
+  if (!two) {
+    grid = ctx.num_sms < a.ntiles ? ctx.num_sms : a.ntiles;
+    if (!choose(kStageTargetOne)) return cudaErrorNotSupported;
+    a.stages = (kOneBudget - act_bytes - rps_one - 1024) / (a.stage_bytes + rps_one);
+    if (a.stages > kMaxStages) a.stages = kMaxStages;
+    if (a.stages < 2) return cudaErrorNotSupported;
+  }
+  const int ncw = two ? kNcwTwo : kNcwOne;
+  a.red_off = a.stages * a.stage_bytes + act_bytes;
+  const size_t smem = (size_t)a.red_off + (size_t)(a.stages + 1) * NWT * ncw * kRows * 4 + 1024;
   a.status = ctx.status;
   a.bias = static_cast<const __half*>(ctx.bias);
   a.bias_mode = PAIR ? 0 : ctx.bias_mode;
 
-  CUtensorMap tm[2];
+  // Tensor maps: packed bytes as [K/256 segments][N rows][128 bytes] (box 128 x 16 x nseg)
+  // and scales as [srow/128][N][128] (box 128 x 16 x nsbox) when the scale rows are whole
+  // 128 bytes, else [N][srow] (box 128 x 16 per copy, the row tail read as zeros).
+  a.s3d = srow % 128 == 0 ? 1 : 0;
+  CUtensorMap tp[2], ts[2];
   for (int t = 0; t < 2; ++t) {
-    memset(&tm[t], 0, sizeof(CUtensorMap));
+    memset(&tp[t], 0, sizeof(CUtensorMap));
+    memset(&ts[t], 0, sizeof(CUtensorMap));
     const QWeight& q = w[t < NWT ? t : 0];
-    const cuuint64_t gdim[2] = {(cuuint64_t)srow, (cuuint64_t)N};
-    const cuuint64_t gstride[1] = {(cuuint64_t)srow};
-    const cuuint32_t box[2] = {128, (cuuint32_t)kRows};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&tm[t], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(q.scales), gdim, gstride, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint64_t pdim[3] = {128, (cuuint64_t)N, (cuuint64_t)(K / kBlockK)};
+    const cuuint64_t pstride[2] = {(cuuint64_t)(K / 2), 128};
+    const cuuint32_t pbox[3] = {128, (cuuint32_t)kRows, (cuuint32_t)a.nseg};
+    if (encode(&tp[t], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(q.packed), pdim, pstride, pbox, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorNotSupported;
+    CUresult r;
+    if (a.s3d) {
+      const cuuint64_t sdim[3] = {128, (cuuint64_t)N, (cuuint64_t)(srow / 128)};
+      const cuuint64_t sstride[2] = {(cuuint64_t)srow, 128};
+      const cuuint32_t sbox[3] = {128, (cuuint32_t)kRows, (cuuint32_t)a.nsbox};
+      r = encode(&ts[t], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q.scales), sdim, sstride, sbox, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+      const cuuint64_t sdim[2] = {(cuuint64_t)srow, (cuuint64_t)N};
+      const cuuint64_t sstride[1] = {(cuuint64_t)srow};
+      const cuuint32_t sbox[2] = {128, (cuuint32_t)kRows};
+      r = encode(&ts[t], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(q.scales), sdim, sstride, sbox, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return cudaErrorNotSupported;
   }
   const int cpg = bs / 32;
-  MmaKernel kern = half_sm ? pick<8, PAIR>(s16, zp, cpg) : pick<16, PAIR>(s16, zp, cpg);
+  MmaKernel kern = two ? pick<true, PAIR>(s16, zp, cpg) : pick<false, PAIR>(s16, zp, cpg);
   if (kern == nullptr) return cudaErrorNotSupported;
-  const size_t smem = (size_t)a.stages * a.stage_bytes + act_bytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int threads = ((half_sm ? 8 : 16) + 1) * 32;
   ctx.variant = PAIR ? "gemv_pair_swiglu_mma" : "gemv_mma";
-  return launch_kernel(ctx, kern, dim3(grid), dim3(threads), smem, a, tm[0], tm[1]);
+  return launch_kernel(ctx, kern, dim3(grid), dim3((ncw + 1) * 32), smem, a, tp[0], tp[1], ts[0], ts[1]);
 }
 
 }  // namespace

@@ -84,7 +84,7 @@ GEMV_CASES = [
     ("gv_bs16_mid", 2048, 301, 16, "f16", True, "normal", "gemv_tma_ring"),
     ("gv_k8192", 8192, 300, 64, "f16", True, "normal", "gemv_mma"),
     ("gv_k16384", 16384, 100, 32, "f32", True, "normal", "gemv_tma_ring"),  # zero points, no K slices
-    ("gv_k32768", 32768, 70, 128, "f16", False, "normal", "gemv_mma"),  # four K slices
+    ("gv_k32768", 32768, 70, 128, "f16", False, "normal", "gemv_mma"),  # K slices, one CTA per SM
     ("gv_generic_k48", 48, 5, 16, "f16", True, "normal", "generic"),
     ("gv_generic_k65536", 65536, 9, 64, "f16", True, "normal", "generic"),
     # zero-point rows that are not 16-byte multiples (4, 28, 56 bytes)
