@@ -124,10 +124,10 @@ __device__ __forceinline__ void load_scales(uint32_t addr, float& s0, float& s1)
   }
 }
 
-// CPG: 32-k chunks per quant group (1, 2, 4 for block sizes 32, 64, 128).  TWO: two CTAs
-// share an SM (launch bounds that leave each at most half the registers).
-template <int NCW, bool TWO, bool PAIR, bool S16, bool ZP, int CPG>
-__global__ void __launch_bounds__((NCW + 1) * 32, TWO ? 2 : 1)
+// CPG: 32-k chunks per quant group (1, 2, 4 for block sizes 32, 64, 128).  CPS: CTAs that
+// share an SM (launch bounds leave each at most 1 / CPS of the registers).
+template <int NCW, int CPS, bool PAIR, bool S16, bool ZP, int CPG>
+__global__ void __launch_bounds__((NCW + 1) * 32, CPS)
     gemv_mma_kernel(const MmaGemvArgs p, const __grid_constant__ CUtensorMap tmp0,
                     const __grid_constant__ CUtensorMap tmp1, const __grid_constant__ CUtensorMap tms0,
                     const __grid_constant__ CUtensorMap tms1) {
@@ -162,6 +162,28 @@ __global__ void __launch_bounds__((NCW + 1) * 32, TWO ? 2 : 1)
   }
   __syncthreads();
 
+  // Requests stage st (tile, weight, K slice) into ring slot `slot`.
+  auto issue = [&](int st, int slot) {
+    const int r = st % nsub;
+    const int ti = t_begin + st / nsub, wt = r / p.nslices, si = r % p.nslices;
+    const int n0 = ti * kRows, nr = min(kRows, p.N - n0);
+    const int klen = min(p.kslice, p.K - si * p.kslice);
+    const int nsb = p.s3d ? p.nsbox : (((klen / (32 * CPG)) * kSsz + 127) >> 7);
+    const uint32_t bytes = (uint32_t)((p.nseg + nsb) * kBoxBytes) + (uint32_t)(ZP ? nr * p.zrow : 0);
+    const bool w1 = NWT == 2 && wt == 1;
+    uint8_t* wb = ring + (size_t)slot * p.stage_bytes;
+    mbar_arrive_expect_tx(&full_bar[slot], bytes);
+    // rows past N and segments past K arrive as zeros (and count in full)
+    tc::tma_load_3d(wb + p.poff, w1 ? &tmp1 : &tmp0, 0, n0, si * bps, &full_bar[slot]);
+    if (p.s3d)
+      tc::tma_load_3d(wb, w1 ? &tms1 : &tms0, 0, n0, (si * p.sslice) >> 7, &full_bar[slot]);
+    else
+      for (int b = 0; b < nsb; ++b)
+        tc::tma_load_2d(wb + b * kBoxBytes, w1 ? &tms1 : &tms0, si * p.sslice + b * 128, n0, &full_bar[slot]);
+    if (ZP)
+      bulk_g2s(wb + p.zoff, (w1 ? p.zp[1] : p.zp[0]) + (long long)n0 * p.zrow, (uint32_t)(nr * p.zrow),
+               &full_bar[slot]);
+  };
   if (warp == NCW) {
     // ------------------------------- producer -------------------------------------
     if (lane == 0) {
@@ -173,25 +195,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, TWO ? 2 : 1)
           atomicExch(&failed, 1);
           break;
         }
-        const int r = st % nsub;
-        const int ti = t_begin + st / nsub, wt = r / p.nslices, si = r % p.nslices;
-        const int n0 = ti * kRows, nr = min(kRows, p.N - n0);
-        const int klen = min(p.kslice, p.K - si * p.kslice);
-        const int nsb = p.s3d ? p.nsbox : (((klen / (32 * CPG)) * kSsz + 127) >> 7);
-        const uint32_t bytes = (uint32_t)((p.nseg + nsb) * kBoxBytes) + (uint32_t)(ZP ? nr * p.zrow : 0);
-        const bool w1 = NWT == 2 && wt == 1;
-        uint8_t* wb = ring + (size_t)slot * p.stage_bytes;
-        mbar_arrive_expect_tx(&full_bar[slot], bytes);
-        // rows past N and segments past K arrive as zeros (and count in full)
-        tc::tma_load_3d(wb + p.poff, w1 ? &tmp1 : &tmp0, 0, n0, si * bps, &full_bar[slot]);
-        if (p.s3d)
-          tc::tma_load_3d(wb, w1 ? &tms1 : &tms0, 0, n0, (si * p.sslice) >> 7, &full_bar[slot]);
-        else
-          for (int b = 0; b < nsb; ++b)
-            tc::tma_load_2d(wb + b * kBoxBytes, w1 ? &tms1 : &tms0, si * p.sslice + b * 128, n0, &full_bar[slot]);
-        if (ZP)
-          bulk_g2s(wb + p.zoff, (w1 ? p.zp[1] : p.zp[0]) + (long long)n0 * p.zrow, (uint32_t)(nr * p.zrow),
-                   &full_bar[slot]);
+        issue(st, slot);
         issued = st + 1;
         if (++slot == S) {
           slot = 0;
@@ -397,22 +401,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, TWO ? 2 : 1)
 using MmaKernel = void (*)(const MmaGemvArgs, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                            const CUtensorMap);
 
-// Consumer warps: 8 when two CTAs share an SM (at most half its registers each), else 16.
+// Consumer warps: 8 when two CTAs share an SM, else 16.
 constexpr int kNcwTwo = 8, kNcwOne = 16;
 
-template <bool TWO, bool PAIR, bool S16, bool ZP>
+template <int CPS, bool PAIR, bool S16, bool ZP>
 MmaKernel pick_cpg(int cpg) {
-  constexpr int NCW = TWO ? kNcwTwo : kNcwOne;
-  if (cpg == 1) return gemv_mma_kernel<NCW, TWO, PAIR, S16, ZP, 1>;
-  if (cpg == 2) return gemv_mma_kernel<NCW, TWO, PAIR, S16, ZP, 2>;
-  if (cpg == 4) return gemv_mma_kernel<NCW, TWO, PAIR, S16, ZP, 4>;
+  constexpr int NCW = CPS > 1 ? kNcwTwo : kNcwOne;
+  if (cpg == 1) return gemv_mma_kernel<NCW, CPS, PAIR, S16, ZP, 1>;
+  if (cpg == 2) return gemv_mma_kernel<NCW, CPS, PAIR, S16, ZP, 2>;
+  if (cpg == 4) return gemv_mma_kernel<NCW, CPS, PAIR, S16, ZP, 4>;
   return nullptr;
 }
 
-template <bool TWO, bool PAIR>
+template <int CPS, bool PAIR>
 MmaKernel pick(bool s16, bool zp, int cpg) {
-  if (s16) return zp ? pick_cpg<TWO, PAIR, true, true>(cpg) : pick_cpg<TWO, PAIR, true, false>(cpg);
-  return zp ? pick_cpg<TWO, PAIR, false, true>(cpg) : pick_cpg<TWO, PAIR, false, false>(cpg);
+  if (s16) return zp ? pick_cpg<CPS, PAIR, true, true>(cpg) : pick_cpg<CPS, PAIR, true, false>(cpg);
+  return zp ? pick_cpg<CPS, PAIR, false, true>(cpg) : pick_cpg<CPS, PAIR, false, false>(cpg);
 }
 
 // Dynamic shared memory per CTA when two CTAs share an SM, and when one CTA has the SM; the
@@ -477,21 +481,18 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
     return true;
   };
   // Launch shape, in order of preference:
-  //  * two CTAs per SM, one CTA per SM per call, when all of a CTA's stages fit half an SM:
-  //    every weight byte is requested at once and the next call's CTA streams its weights
-  //    while this call computes;
+  //  * two CTAs per SM, one CTA per SM per call, when all of a CTA's stages fit half an SM;
   //  * two CTAs of the same call per SM when stages of at least kTwoMinStage fit half an SM
   //    (two stages in flight per CTA, sixteen warps computing per SM);
   //  * else one CTA per SM with sixteen consumer warps and a deeper ring.
   // each stage also needs one tile-sum slot (plus one spare slot)
   const int rps_two = NWT * kNcwTwo * kRows * 4, rps_one = NWT * kNcwOne * kRows * 4;
+  int grid = 0, cps = 0;
   const int avail = kTwoBudget - act_bytes - rps_two - 1024;
-  int grid = 0;
-  bool two = false;
-  for (int mult = 1; mult <= 2 && !two; ++mult) {
+  for (int mult = 1; mult <= 2 && cps == 0; ++mult) {
     const int g = ctx.num_sms * mult < a.ntiles ? ctx.num_sms * mult : a.ntiles;
     const int max_tiles = (a.ntiles + g - 1) / g;
-    for (int want = 3; want >= 2 && !two && avail > 0; --want) {
+    for (int want = 3; want >= 2 && cps == 0 && avail > 0; --want) {
       const int target = avail / want - rps_two < kStageTargetTwo ? avail / want - rps_two : kStageTargetTwo;
       if (!choose(target)) continue;
       const int need = max_tiles * NWT * a.nslices;  // stages of the busiest CTA
@@ -500,19 +501,21 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
       if (stages > need) stages = need;
       const bool all_fit = stages >= 1 && stages == need;
       if ((mult == 1 && all_fit) || (mult == 2 && stages >= 2 && a.stage_bytes >= kTwoMinStage)) {
-        two = true;
+        cps = 2;
         grid = g;
         a.stages = stages;
       }
     }
   }
-  if (!two) {
+  if (cps == 0) {
+    cps = 1;
     grid = ctx.num_sms < a.ntiles ? ctx.num_sms : a.ntiles;
     if (!choose(kStageTargetOne)) return cudaErrorNotSupported;
     a.stages = (kOneBudget - act_bytes - rps_one - 1024) / (a.stage_bytes + rps_one);
     if (a.stages > kMaxStages) a.stages = kMaxStages;
     if (a.stages < 2) return cudaErrorNotSupported;
   }
+  const bool two = cps > 1;
   const int ncw = two ? kNcwTwo : kNcwOne;
   a.red_off = a.stages * a.stage_bytes + act_bytes;
   const size_t smem = (size_t)a.red_off + (size_t)(a.stages + 1) * NWT * ncw * kRows * 4 + 1024;
@@ -556,12 +559,15 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
     if (r != CUDA_SUCCESS) return cudaErrorNotSupported;
   }
   const int cpg = bs / 32;
-  MmaKernel kern = two ? pick<true, PAIR>(s16, zp, cpg) : pick<false, PAIR>(s16, zp, cpg);
+  MmaKernel kern = nullptr;
+  if (cps == 2) kern = pick<2, PAIR>(s16, zp, cpg);
+  if (cps == 1) kern = pick<1, PAIR>(s16, zp, cpg);
   if (kern == nullptr) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ctx.variant = PAIR ? "gemv_pair_swiglu_mma" : "gemv_mma";
-  return launch_kernel(ctx, kern, dim3(grid), dim3((ncw + 1) * 32), smem, a, tp[0], tp[1], ts[0], ts[1]);
+  const int threads = (ncw + 1) * 32;
+  return launch_kernel(ctx, kern, dim3(grid), dim3(threads), smem, a, tp[0], tp[1], ts[0], ts[1]);
 }
 
 }  // namespace
