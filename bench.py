@@ -659,7 +659,8 @@ def main():
 
     gbps_total = head["gbps"] * world
     hbm = float(peaks["hbm_gbs"])
-    gemv_files = ["gemm_mnb_gemv_gb300/csrc/gemv_tma.cu", "gemm_mnb_gemv_gb300/csrc/mnb_device.cuh"]
+    gemv_files = ["gemm_mnb_gemv_gb300/csrc/gemv_mma.cu", "gemm_mnb_gemv_gb300/csrc/mma_sync.cuh",
+                  "gemm_mnb_gemv_gb300/csrc/mnb_device.cuh", "gemm_mnb_gemv_gb300/csrc/tcgen05.cuh"]
     roof = {"bound": "hbm", "achieved": head["gbps"], "peak": hbm, "unit": "GB/s",
             "frac": head["gbps"] / hbm, "traffic": profiled_traffic("gemv_attnproj", gemv_files),
             "algorithmic_bytes_per_launch": call_bytes(wl), "kernel": head["variant"],
