@@ -184,6 +184,26 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
       bulk_g2s(wb + p.zoff, (w1 ? p.zp[1] : p.zp[0]) + (long long)n0 * p.zrow, (uint32_t)(nr * p.zrow),
                &full_bar[slot]);
   };
+  // Adds the consumer warps' posted partials of tile tl (slot rp) in warp order and stores
+  // the tile's outputs (lanes 0..15).
+  auto store_tile = [&](int tl, const float* rp) {
+    const int n = (t_begin + tl) * kRows + lane;
+    if (lane < kRows && n < p.N) {
+      float v[NWT];
+#pragma unroll
+      for (int w = 0; w < NWT; ++w) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int ww = 0; ww < NCW; ++ww) sum += *(volatile const float*)&rp[(w * NCW + ww) * kRows + lane];
+        v[w] = sum;
+      }
+      __half out;
+      if constexpr (PAIR) out = __float2half_rn(silu_f32(v[0]) * v[1]);
+      else out = round_out(v[0], p.bias, n, p.bias_mode);
+      if (*(volatile int*)&failed) out = __ushort_as_half(0x7e00);
+      reinterpret_cast<__half*>(p.Y)[n] = out;
+    }
+  };
   if (warp == NCW) {
     // ------------------------------- producer -------------------------------------
     if (lane == 0) {
@@ -253,112 +273,122 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
     __syncwarp();
 
     const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
-    float acc[NWT][2];
+    const int ntl = t_end - t_begin;
+    // Tile sums.  With at most S + 1 tiles every tile has its own slot, and the warps'
+    // partials are added once after the last tile (no per-tile synchronisation).  Otherwise
+    // slots are reused every S + 1 tiles and the last warp to post a tile adds and stores it;
+    // the ring slot of a tile's last stage is released only after the post, so no warp can be
+    // S + 1 tiles ahead of the warp that reads a slot.
+    const bool deferred = ntl <= S + 1;
     bool ok = true;
     int slot = 0;
     uint32_t phase = 0;
-    for (int st = 0; st < nst; ++st) {
-      const int tl = st / nsub, r = st % nsub;
-      const int wt = r / p.nslices, si = r % p.nslices;
-      if (r == 0) {
+    for (int tl = 0; tl < ntl; ++tl) {
+      float acc[NWT][2];
+      int last_slot = 0;
 #pragma unroll
-        for (int w = 0; w < NWT; ++w) acc[w][0] = acc[w][1] = 0.0f;
-      }
-      if (ok && !mbar_wait_bounded(&full_bar[slot], phase)) {
-        report_status(p.status, kStatusFullWait);
-        atomicExch(&failed, 1);
-        ok = false;
-      }
-      const uint32_t wbase = ring_u32 + (uint32_t)(slot * p.stage_bytes);
-      const int nb = (min(p.kslice, p.K - si * p.kslice)) / kBlockK;
-      const int b_lo = (warp * nb) / NCW, b_hi = ok ? ((warp + 1) * nb) / NCW : b_lo;
-      float vg = 0.0f, v8 = 0.0f;  // this stage's partial sums of rows g and g + 8
-      for (int b = b_lo; b < b_hi; ++b) {
-        const uint32_t abase = act_u32 + (uint32_t)((si * bps + b) * 512 + g * 16);
-        const int o0 = so0 + sos * b;  // scale byte within the slice's boxes
-        const uint32_t soff = (uint32_t)((o0 >> 7) * kBoxBytes + g * 128 + ((((o0 & 127) >> 4) ^ g) << 4) + (o0 & 15));
-        // segment b, row g, 16-byte units 2t (X) and 2t + 1 (Y) swizzled by the row; row g + 8
-        // 1024 bytes on, same swizzle
-        const uint32_t seg = wbase + (uint32_t)(p.poff + b * kBoxBytes + g * 128);
-        const uint32_t rxa = seg + (uint32_t)(((2 * t) ^ g) << 4), rya = seg + (uint32_t)(((2 * t + 1) ^ g) << 4);
-        uint32_t bq[4][4];
+      for (int wt = 0; wt < NWT; ++wt) {
+        acc[wt][0] = acc[wt][1] = 0.0f;
+        for (int si = 0; si < p.nslices; ++si) {
+          if (ok && !mbar_wait_bounded(&full_bar[slot], phase)) {
+            report_status(p.status, kStatusFullWait);
+            atomicExch(&failed, 1);
+            ok = false;
+          }
+          const uint32_t wbase = ring_u32 + (uint32_t)(slot * p.stage_bytes);
+          const int nb = (min(p.kslice, p.K - si * p.kslice)) / kBlockK;
+          const int b_lo = (warp * nb) / NCW, b_hi = ok ? ((warp + 1) * nb) / NCW : b_lo;
+          float vg = 0.0f, v8 = 0.0f;  // this stage's partial sums of rows g and g + 8
+          for (int b = b_lo; b < b_hi; ++b) {
+            const uint32_t abase = act_u32 + (uint32_t)((si * bps + b) * 512 + g * 16);
+            const int o0 = so0 + sos * b;  // scale byte within the slice's boxes
+            const uint32_t soff = (uint32_t)((o0 >> 7) * kBoxBytes + g * 128 + ((((o0 & 127) >> 4) ^ g) << 4) + (o0 & 15));
+            // segment b, row g, 16-byte units 2t (X) and 2t + 1 (Y) swizzled by the row; row g + 8
+            // 1024 bytes on, same swizzle
+            const uint32_t seg = wbase + (uint32_t)(p.poff + b * kBoxBytes + g * 128);
+            const uint32_t rxa = seg + (uint32_t)(((2 * t) ^ g) << 4), rya = seg + (uint32_t)(((2 * t + 1) ^ g) << 4);
+            uint32_t bq[4][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          bq[q][0] = bq[q][1] = bq[q][2] = bq[q][3] = 0u;
-          lds128_pred(bq[q], abase + (uint32_t)(q * 128), bdata);
-        }
-        const uint4 xa = lds128_a(rxa), ya = lds128_a(rya);
-        const uint4 xb = lds128_a(rxa + 1024u), yb = lds128_a(rya + 1024u);
-        float sa0, sa1, sb0, sb1;
-        load_scales<S16, CPG>(wbase + soff, sa0, sa1);
-        load_scales<S16, CPG>(wbase + soff + 1024u, sb0, sb1);  // row g + 8: same swizzle
-        uint32_t zlxa = zl8, zhxa = zh8, zlya = zl8, zhya = zh8;
-        uint32_t zlxb = zl8, zhxb = zh8, zlyb = zl8, zhyb = zh8;
-        if constexpr (ZP) {
-          const uint32_t zaddr = wbase + (uint32_t)(p.zoff + g * p.zrow + zb0 + zbs * b);
-          const uint32_t za = lds_u8_a(zaddr), zb = lds_u8_a(zaddr + (uint32_t)(8 * p.zrow));
-          const uint32_t za0 = (za >> zsh0) & 15u, za1 = (za >> zsh1) & 15u;
-          const uint32_t zb0v = (zb >> zsh0) & 15u, zb1v = (zb >> zsh1) & 15u;
-          zlxa = zp_lo_const(za0);
-          zhxa = zp_hi_const(za0);
-          zlya = zp_lo_const(za1);
-          zhya = zp_hi_const(za1);
-          zlxb = zp_lo_const(zb0v);
-          zhxb = zp_hi_const(zb0v);
-          zlyb = zp_lo_const(zb1v);
-          zhyb = zp_hi_const(zb1v);
-        }
-        float dx0[4], dx1[4], dy0[4], dy1[4];
+            for (int q = 0; q < 4; ++q) {
+              bq[q][0] = bq[q][1] = bq[q][2] = bq[q][3] = 0u;
+              lds128_pred(bq[q], abase + (uint32_t)(q * 128), bdata);
+            }
+            const uint4 xa = lds128_a(rxa), ya = lds128_a(rya);
+            const uint4 xb = lds128_a(rxa + 1024u), yb = lds128_a(rya + 1024u);
+            float sa0, sa1, sb0, sb1;
+            load_scales<S16, CPG>(wbase + soff, sa0, sa1);
+            load_scales<S16, CPG>(wbase + soff + 1024u, sb0, sb1);  // row g + 8: same swizzle
+            uint32_t zlxa = zl8, zhxa = zh8, zlya = zl8, zhya = zh8;
+            uint32_t zlxb = zl8, zhxb = zh8, zlyb = zl8, zhyb = zh8;
+            if constexpr (ZP) {
+              const uint32_t zaddr = wbase + (uint32_t)(p.zoff + g * p.zrow + zb0 + zbs * b);
+              const uint32_t za = lds_u8_a(zaddr), zb = lds_u8_a(zaddr + (uint32_t)(8 * p.zrow));
+              const uint32_t za0 = (za >> zsh0) & 15u, za1 = (za >> zsh1) & 15u;
+              const uint32_t zb0v = (zb >> zsh0) & 15u, zb1v = (zb >> zsh1) & 15u;
+              zlxa = zp_lo_const(za0);
+              zhxa = zp_hi_const(za0);
+              zlya = zp_lo_const(za1);
+              zhya = zp_hi_const(za1);
+              zlxb = zp_lo_const(zb0v);
+              zhxb = zp_hi_const(zb0v);
+              zlyb = zp_lo_const(zb1v);
+              zhyb = zp_hi_const(zb1v);
+            }
+            float dx0[4], dx1[4], dy0[4], dy1[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t da[4], db[4], ea[4], eb[4];
-          nibbles_to_centered_half2(word_of(xa, q), zlxa, zhxa, da);
-          nibbles_to_centered_half2(word_of(xb, q), zlxb, zhxb, db);
-          nibbles_to_centered_half2(word_of(ya, q), zlya, zhya, ea);
-          nibbles_to_centered_half2(word_of(yb, q), zlyb, zhyb, eb);
-          if (q == 0) {
-            mma16816_zero(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
-            mma16816_zero(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
-            mma16816_zero(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
-            mma16816_zero(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
+            for (int q = 0; q < 4; ++q) {
+              uint32_t da[4], db[4], ea[4], eb[4];
+              nibbles_to_centered_half2(word_of(xa, q), zlxa, zhxa, da);
+              nibbles_to_centered_half2(word_of(xb, q), zlxb, zhxb, db);
+              nibbles_to_centered_half2(word_of(ya, q), zlya, zhya, ea);
+              nibbles_to_centered_half2(word_of(yb, q), zlyb, zhyb, eb);
+              if (q == 0) {
+                mma16816_zero(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
+                mma16816_zero(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
+                mma16816_zero(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
+                mma16816_zero(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
+              } else {
+                mma16816(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
+                mma16816(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
+                mma16816(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
+                mma16816(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
+              }
+            }
+            // lane (g, t): X column 2t (registers 0, 2) and Y column 2t + 1 (registers 1, 3)
+            vg = fmaf(dx0[0] + dx1[0], sa0, vg);
+            vg = fmaf(dy0[1] + dy1[1], sa1, vg);
+            v8 = fmaf(dx0[2] + dx1[2], sb0, v8);
+            v8 = fmaf(dy0[3] + dy1[3], sb1, v8);
+          }
+          acc[wt][0] += vg;
+          acc[wt][1] += v8;
+          if (wt == NWT - 1 && si == p.nslices - 1) {
+            last_slot = slot;
           } else {
-            mma16816(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
-            mma16816(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
-            mma16816(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
-            mma16816(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[slot]);  // this warp no longer reads the slot
+          }
+          if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
           }
         }
-        // lane (g, t): X column 2t (registers 0, 2) and Y column 2t + 1 (registers 1, 3)
-        vg = fmaf(dx0[0] + dx1[0], sa0, vg);
-        vg = fmaf(dy0[1] + dy1[1], sa1, vg);
-        v8 = fmaf(dx0[2] + dx1[2], sb0, v8);
-        v8 = fmaf(dy0[3] + dy1[3], sb1, v8);
       }
-      if (NWT == 1 || wt == 0) {
-        acc[0][0] += vg;
-        acc[0][1] += v8;
-      } else {
-        acc[NWT - 1][0] += vg;
-        acc[NWT - 1][1] += v8;
-      }
-      if (r == nsub - 1) {
-        // The tile is done: sum the four lanes of each row and post this warp's partials;
-        // the last warp to post adds the warps' partials in warp order and stores the tile.
-        // Slots are reused every S + 1 tiles; the slot of this stage is released only after
-        // this, so no warp can be S + 1 tiles ahead of the warp that reads a slot.
-        const int rs = tl % (S + 1);
-        float* rp = red + (size_t)rs * (NWT * NCW * kRows);
+      // Sum the four lanes of each row and post this warp's partials of the tile.
+      const int rs = deferred ? tl : tl % (S + 1);
+      float* rp = red + (size_t)rs * (NWT * NCW * kRows);
 #pragma unroll
-        for (int w = 0; w < NWT; ++w) {
+      for (int w = 0; w < NWT; ++w) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float x = acc[w][h];
-            x += __shfl_xor_sync(kFull, x, 1);
-            x += __shfl_xor_sync(kFull, x, 2);
-            if (t == 0) rp[(w * NCW + warp) * kRows + g + 8 * h] = x;
-          }
+        for (int h = 0; h < 2; ++h) {
+          float x = acc[w][h];
+          x += __shfl_xor_sync(kFull, x, 1);
+          x += __shfl_xor_sync(kFull, x, 2);
+          if (t == 0) rp[(w * NCW + warp) * kRows + g + 8 * h] = x;
         }
-        __syncwarp();
+      }
+      __syncwarp();
+      if (!deferred) {
         unsigned last = 0;
         if (lane == 0) {
           __threadfence_block();
@@ -367,30 +397,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
         last = __shfl_sync(kFull, last, 0);
         if (last) {
           __threadfence_block();
-          const int n = (t_begin + tl) * kRows + lane;
-          if (lane < kRows && n < p.N) {
-            float v[NWT];
-#pragma unroll
-            for (int w = 0; w < NWT; ++w) {
-              float sum = 0.0f;
-#pragma unroll
-              for (int ww = 0; ww < NCW; ++ww) sum += *(volatile float*)&rp[(w * NCW + ww) * kRows + lane];
-              v[w] = sum;
-            }
-            __half out;
-            if constexpr (PAIR) out = __float2half_rn(silu_f32(v[0]) * v[1]);
-            else out = round_out(v[0], p.bias, n, p.bias_mode);
-            if (*(volatile int*)&failed) out = __ushort_as_half(0x7e00);
-            reinterpret_cast<__half*>(p.Y)[n] = out;
-          }
+          store_tile(tl, rp);
         }
+        __syncwarp();
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[slot]);  // this warp no longer reads the slot
-      if (++slot == S) {
-        slot = 0;
-        phase ^= 1u;
-      }
+      if (lane == 0) mbar_arrive(&empty_bar[last_slot]);
+    }
+    if (deferred) {
+      // every consumer warp has posted every tile: add and store them, one warp per tile
+      asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
+      for (int tl = warp; tl < ntl; tl += NCW) store_tile(tl, red + (size_t)tl * (NWT * NCW * kRows));
     }
   }
 }
