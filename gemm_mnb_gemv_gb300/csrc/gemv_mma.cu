@@ -31,14 +31,17 @@
 //
 // Bank conflicts.  In a swizzled segment the 8 lanes of a quarter-warp (rows g, g + 1,
 // chunk 2t or 2t + 1) read 8 different 16-byte units; rows g and g + 8 share a swizzle.
-// The activation is staged once per CTA (after the programmatic-launch wait; each warp
-// stages only the blocks it uses, so no CTA-wide barrier) in MMA order: block kb, step q,
-// chunk c at byte (kb * 32 + q * 8 + c) * 16, the 8 halves paired as the conversion pairs
-// nibbles.
+// The activation (K <= 8192) is staged once per CTA after the programmatic-launch wait, each
+// warp only the blocks it uses (no CTA-wide barrier), in MMA order with the 8 halves of a
+// step paired as the conversion pairs nibbles.  A larger one is not staged, so the weight
+// stages keep the shared memory: each warp requests the lines of its blocks into L1, and
+// the 8 lanes that carry B load their chunk (64 contiguous bytes per block) and pair it.
 //
 // Tile sums.  After a tile each warp sums its four lanes per row and posts the partials of
-// its 16 rows; the last warp to post (a shared-memory counter) adds them in warp order and
-// stores the tile, so no warp waits on the others.
+// its 16 rows.  When a CTA has at most S + 1 tiles (S ring stages) each tile has its own
+// slot and one warp per tile adds and stores the posted partials after a barrier of the
+// consumer warps at the end; otherwise the last warp to post a tile (a shared-memory
+// counter) adds and stores it, so no warp waits on the others.
 //
 // Launch overlap.  When a CTA's whole share fits half an SM (8 consumer warps, at most half
 // the SM's registers and shared memory each), one CTA per SM per call: the next call's CTA
@@ -80,11 +83,19 @@ struct MmaGemvArgs {
   int poff, zoff;    // packed segments and zero points inside a stage
   int stage_bytes;   // one stage: one weight's tile slice (multiple of 1024)
   int stages;
-  int red_off;       // tile-sum slots after the activation: [stages + 1][weights][warps][16]
+  int act_smem;      // 1: the activation is staged after the stages (K * 2 bytes), 0: read from L1/L2
+  int red_off;       // tile-sum slots after the stages (and the activation): [stages + 1][weights][warps][16]
   int ntiles;
   uint32_t* status;
   const __half* bias;
   int bias_mode;
+};
+
+// One block's weight side for one lane: A fragments of the 16 MMAs (per step q: X rows g,
+// g + 8, then Y rows g, g + 8, four registers each) and the scales of its two chunks.
+struct BlockFrag {
+  uint32_t w[4][16];
+  float sa0, sa1, sb0, sb1;
 };
 
 __device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
@@ -125,8 +136,9 @@ __device__ __forceinline__ void load_scales(uint32_t addr, float& s0, float& s1)
 }
 
 // CPG: 32-k chunks per quant group (1, 2, 4 for block sizes 32, 64, 128).  CPS: CTAs that
-// share an SM (launch bounds leave each at most 1 / CPS of the registers).
-template <int NCW, int CPS, bool PAIR, bool S16, bool ZP, int CPG>
+// share an SM (launch bounds leave each at most 1 / CPS of the registers).  ASM: the
+// activation is staged in shared memory.
+template <int NCW, int CPS, bool PAIR, bool S16, bool ZP, int CPG, bool ASM>
 __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
     gemv_mma_kernel(const MmaGemvArgs p, const __grid_constant__ CUtensorMap tmp0,
                     const __grid_constant__ CUtensorMap tmp1, const __grid_constant__ CUtensorMap tms0,
@@ -242,45 +254,144 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
     const uint32_t zsh1 = CPG == 1 ? 4u : zsh0;
     const int so0 = (CPG == 1 ? 2 * t : (CPG == 2 ? t : (t >> 1))) * kSsz;
     const int sos = (CPG == 1 ? 8 : (CPG == 2 ? 4 : 2)) * kSsz;
-    pdl_wait();
-    // Stage this warp's activation blocks in MMA order (lane l holds halves 8l .. 8l + 7 of
-    // a block: chunk l / 4, step l % 4).
-    for (int si = 0; si < p.nslices; ++si) {
-      const int nb = (min(p.kslice, p.K - si * p.kslice)) / kBlockK;
-      const int b_lo = (warp * nb) / NCW, b_hi = ((warp + 1) * nb) / NCW;
-      for (int b0 = b_lo; b0 < b_hi; b0 += 4) {
-        uint4 x[4];
+    const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
+    // Block b of the stage at wbase, weight side: rows g and g + 8, chunks 2t (X) and 2t + 1
+    // (Y), converted to the MMA's A fragments, and their scales.
+    auto prep = [&](uint32_t wbase, int b, BlockFrag& f) {
+      const int o0 = so0 + sos * b;  // scale byte within the slice's boxes
+      const uint32_t soff = (uint32_t)((o0 >> 7) * kBoxBytes + g * 128 + ((((o0 & 127) >> 4) ^ g) << 4) + (o0 & 15));
+      // segment b, row g, 16-byte units 2t (X) and 2t + 1 (Y) swizzled by the row; row g + 8
+      // 1024 bytes on, same swizzle
+      const uint32_t seg = wbase + (uint32_t)(p.poff + b * kBoxBytes + g * 128);
+      const uint32_t rxa = seg + (uint32_t)(((2 * t) ^ g) << 4), rya = seg + (uint32_t)(((2 * t + 1) ^ g) << 4);
+      const uint4 xa = lds128_a(rxa), ya = lds128_a(rya);
+      const uint4 xb = lds128_a(rxa + 1024u), yb = lds128_a(rya + 1024u);
+      load_scales<S16, CPG>(wbase + soff, f.sa0, f.sa1);
+      load_scales<S16, CPG>(wbase + soff + 1024u, f.sb0, f.sb1);  // row g + 8: same swizzle
+      uint32_t zlxa = zl8, zhxa = zh8, zlya = zl8, zhya = zh8;
+      uint32_t zlxb = zl8, zhxb = zh8, zlyb = zl8, zhyb = zh8;
+      if constexpr (ZP) {
+        const uint32_t zaddr = wbase + (uint32_t)(p.zoff + g * p.zrow + zb0 + zbs * b);
+        const uint32_t za = lds_u8_a(zaddr), zb = lds_u8_a(zaddr + (uint32_t)(8 * p.zrow));
+        const uint32_t za0 = (za >> zsh0) & 15u, za1 = (za >> zsh1) & 15u;
+        const uint32_t zb0v = (zb >> zsh0) & 15u, zb1v = (zb >> zsh1) & 15u;
+        zlxa = zp_lo_const(za0);
+        zhxa = zp_hi_const(za0);
+        zlya = zp_lo_const(za1);
+        zhya = zp_hi_const(za1);
+        zlxb = zp_lo_const(zb0v);
+        zhxb = zp_hi_const(zb0v);
+        zlyb = zp_lo_const(zb1v);
+        zhyb = zp_hi_const(zb1v);
+      }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          x[u] = make_uint4(0, 0, 0, 0);
-          const int kb = si * bps + b0 + u;
-          if (b0 + u < b_hi) x[u] = *reinterpret_cast<const uint4*>(p.A + (long long)kb * kBlockK + 8 * lane);
+      for (int q = 0; q < 4; ++q) {
+        nibbles_to_centered_half2(word_of(xa, q), zlxa, zhxa, f.w[q] + 0);
+        nibbles_to_centered_half2(word_of(xb, q), zlxb, zhxb, f.w[q] + 4);
+        nibbles_to_centered_half2(word_of(ya, q), zlya, zhya, f.w[q] + 8);
+        nibbles_to_centered_half2(word_of(yb, q), zlyb, zhyb, f.w[q] + 12);
+      }
+    };
+    // The activation side of 256-k block kb and the MMAs; adds the scaled partial dots of
+    // rows g and g + 8 into vg and v8.  B column g holds chunk g of the block (halves 32g ..
+    // 32g + 31; step q its 8 halves from 32g + 8q), paired as the conversion pairs nibbles,
+    // on the lanes with g / 2 == t; the other lanes hold zeros.  Staged in shared memory, the
+    // block sits in MMA order: step q, chunk c at byte (kb * 32 + q * 8 + c) * 16.
+    auto finish = [&](int kb, const BlockFrag& f, float& vg, float& v8) {
+      uint32_t bq[4][4];
+      if constexpr (ASM) {
+        const uint32_t abase = act_u32 + (uint32_t)(kb * 512 + g * 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          bq[q][0] = bq[q][1] = bq[q][2] = bq[q][3] = 0u;
+          lds128_pred(bq[q], abase + (uint32_t)(q * 128), bdata);
+        }
+      } else {
+        uint4 av[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) av[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (bdata) {
+          const uint4* ap = reinterpret_cast<const uint4*>(p.A + (long long)kb * kBlockK + 32 * g);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) av[q] = ap[q];
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (b0 + u < b_hi) {
+        for (int q = 0; q < 4; ++q) pair_halves_stride4(av[q], bq[q]);
+      }
+      float dx0[4], dx1[4], dy0[4], dy1[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t* da = f.w[q];
+        const uint32_t* db = f.w[q] + 4;
+        const uint32_t* ea = f.w[q] + 8;
+        const uint32_t* eb = f.w[q] + 12;
+        if (q == 0) {
+          mma16816_zero(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
+          mma16816_zero(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
+          mma16816_zero(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
+          mma16816_zero(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
+        } else {
+          mma16816(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
+          mma16816(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
+          mma16816(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
+          mma16816(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
+        }
+      }
+      // lane (g, t): X column 2t (registers 0, 2) and Y column 2t + 1 (registers 1, 3)
+      vg = fmaf(dx0[0] + dx1[0], f.sa0, vg);
+      vg = fmaf(dy0[1] + dy1[1], f.sa1, vg);
+      v8 = fmaf(dx0[2] + dx1[2], f.sb0, v8);
+      v8 = fmaf(dy0[3] + dy1[3], f.sb1, v8);
+    };
+
+    pdl_wait();
+    if constexpr (ASM) {
+      // Stage this warp's activation blocks in MMA order (lane l holds halves 8l .. 8l + 7 of
+      // a block: chunk l / 4, step l % 4).
+      for (int si = 0; si < p.nslices; ++si) {
+        const int nb = (min(p.kslice, p.K - si * p.kslice)) / kBlockK;
+        const int b_lo = (warp * nb) / NCW, b_hi = ((warp + 1) * nb) / NCW;
+        for (int b0 = b_lo; b0 < b_hi; b0 += 4) {
+          uint4 x[4];
+  #pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            x[u] = make_uint4(0, 0, 0, 0);
             const int kb = si * bps + b0 + u;
-            uint32_t q[4];
-            pair_halves_stride4(x[u], q);
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
-                             act_u32 + (uint32_t)((kb * 32 + (lane & 3) * 8 + (lane >> 2)) * 16)),
-                         "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
-                         : "memory");
+            if (b0 + u < b_hi) x[u] = *reinterpret_cast<const uint4*>(p.A + (long long)kb * kBlockK + 8 * lane);
+          }
+  #pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (b0 + u < b_hi) {
+              const int kb = si * bps + b0 + u;
+              uint32_t q[4];
+              pair_halves_stride4(x[u], q);
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                               act_u32 + (uint32_t)((kb * 32 + (lane & 3) * 8 + (lane >> 2)) * 16)),
+                           "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
+                           : "memory");
+            }
           }
         }
       }
+      __syncwarp();
+    } else {
+      // The activation is read from global memory by the lanes that carry B; this warp's lines
+      // are first requested into L1 so that the first conversions overlap their latency.
+      for (int si = 0; si < p.nslices; ++si) {
+        const int nb = (min(p.kslice, p.K - si * p.kslice)) / kBlockK;
+        const int b_lo = (warp * nb) / NCW, b_hi = ((warp + 1) * nb) / NCW;
+        for (int i = lane; i < 4 * (b_hi - b_lo); i += 32)
+          prefetch_l1(p.A + (long long)(si * bps + b_lo) * kBlockK + 64 * i);
+      }
     }
-    __syncwarp();
-
-    const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
     const int ntl = t_end - t_begin;
+    bool ok = true;
     // Tile sums.  With at most S + 1 tiles every tile has its own slot, and the warps'
     // partials are added once after the last tile (no per-tile synchronisation).  Otherwise
     // slots are reused every S + 1 tiles and the last warp to post a tile adds and stores it;
     // the ring slot of a tile's last stage is released only after the post, so no warp can be
     // S + 1 tiles ahead of the warp that reads a slot.
     const bool deferred = ntl <= S + 1;
-    bool ok = true;
     int slot = 0;
     uint32_t phase = 0;
     for (int tl = 0; tl < ntl; ++tl) {
@@ -300,65 +411,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
           const int b_lo = (warp * nb) / NCW, b_hi = ok ? ((warp + 1) * nb) / NCW : b_lo;
           float vg = 0.0f, v8 = 0.0f;  // this stage's partial sums of rows g and g + 8
           for (int b = b_lo; b < b_hi; ++b) {
-            const uint32_t abase = act_u32 + (uint32_t)((si * bps + b) * 512 + g * 16);
-            const int o0 = so0 + sos * b;  // scale byte within the slice's boxes
-            const uint32_t soff = (uint32_t)((o0 >> 7) * kBoxBytes + g * 128 + ((((o0 & 127) >> 4) ^ g) << 4) + (o0 & 15));
-            // segment b, row g, 16-byte units 2t (X) and 2t + 1 (Y) swizzled by the row; row g + 8
-            // 1024 bytes on, same swizzle
-            const uint32_t seg = wbase + (uint32_t)(p.poff + b * kBoxBytes + g * 128);
-            const uint32_t rxa = seg + (uint32_t)(((2 * t) ^ g) << 4), rya = seg + (uint32_t)(((2 * t + 1) ^ g) << 4);
-            uint32_t bq[4][4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              bq[q][0] = bq[q][1] = bq[q][2] = bq[q][3] = 0u;
-              lds128_pred(bq[q], abase + (uint32_t)(q * 128), bdata);
-            }
-            const uint4 xa = lds128_a(rxa), ya = lds128_a(rya);
-            const uint4 xb = lds128_a(rxa + 1024u), yb = lds128_a(rya + 1024u);
-            float sa0, sa1, sb0, sb1;
-            load_scales<S16, CPG>(wbase + soff, sa0, sa1);
-            load_scales<S16, CPG>(wbase + soff + 1024u, sb0, sb1);  // row g + 8: same swizzle
-            uint32_t zlxa = zl8, zhxa = zh8, zlya = zl8, zhya = zh8;
-            uint32_t zlxb = zl8, zhxb = zh8, zlyb = zl8, zhyb = zh8;
-            if constexpr (ZP) {
-              const uint32_t zaddr = wbase + (uint32_t)(p.zoff + g * p.zrow + zb0 + zbs * b);
-              const uint32_t za = lds_u8_a(zaddr), zb = lds_u8_a(zaddr + (uint32_t)(8 * p.zrow));
-              const uint32_t za0 = (za >> zsh0) & 15u, za1 = (za >> zsh1) & 15u;
-              const uint32_t zb0v = (zb >> zsh0) & 15u, zb1v = (zb >> zsh1) & 15u;
-              zlxa = zp_lo_const(za0);
-              zhxa = zp_hi_const(za0);
-              zlya = zp_lo_const(za1);
-              zhya = zp_hi_const(za1);
-              zlxb = zp_lo_const(zb0v);
-              zhxb = zp_hi_const(zb0v);
-              zlyb = zp_lo_const(zb1v);
-              zhyb = zp_hi_const(zb1v);
-            }
-            float dx0[4], dx1[4], dy0[4], dy1[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t da[4], db[4], ea[4], eb[4];
-              nibbles_to_centered_half2(word_of(xa, q), zlxa, zhxa, da);
-              nibbles_to_centered_half2(word_of(xb, q), zlxb, zhxb, db);
-              nibbles_to_centered_half2(word_of(ya, q), zlya, zhya, ea);
-              nibbles_to_centered_half2(word_of(yb, q), zlyb, zhyb, eb);
-              if (q == 0) {
-                mma16816_zero(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
-                mma16816_zero(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
-                mma16816_zero(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
-                mma16816_zero(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
-              } else {
-                mma16816(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
-                mma16816(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
-                mma16816(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
-                mma16816(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
-              }
-            }
-            // lane (g, t): X column 2t (registers 0, 2) and Y column 2t + 1 (registers 1, 3)
-            vg = fmaf(dx0[0] + dx1[0], sa0, vg);
-            vg = fmaf(dy0[1] + dy1[1], sa1, vg);
-            v8 = fmaf(dx0[2] + dx1[2], sb0, v8);
-            v8 = fmaf(dy0[3] + dy1[3], sb1, v8);
+            BlockFrag f;
+            prep(wbase, b, f);
+            finish(si * bps + b, f, vg, v8);
           }
           acc[wt][0] += vg;
           acc[wt][1] += v8;
@@ -420,19 +475,19 @@ using MmaKernel = void (*)(const MmaGemvArgs, const CUtensorMap, const CUtensorM
 // Consumer warps: 8 when two CTAs share an SM, else 16.
 constexpr int kNcwTwo = 8, kNcwOne = 16;
 
-template <int CPS, bool PAIR, bool S16, bool ZP>
+template <int CPS, bool PAIR, bool S16, bool ZP, bool ASM>
 MmaKernel pick_cpg(int cpg) {
   constexpr int NCW = CPS > 1 ? kNcwTwo : kNcwOne;
-  if (cpg == 1) return gemv_mma_kernel<NCW, CPS, PAIR, S16, ZP, 1>;
-  if (cpg == 2) return gemv_mma_kernel<NCW, CPS, PAIR, S16, ZP, 2>;
-  if (cpg == 4) return gemv_mma_kernel<NCW, CPS, PAIR, S16, ZP, 4>;
+  if (cpg == 1) return gemv_mma_kernel<NCW, CPS, PAIR, S16, ZP, 1, ASM>;
+  if (cpg == 2) return gemv_mma_kernel<NCW, CPS, PAIR, S16, ZP, 2, ASM>;
+  if (cpg == 4) return gemv_mma_kernel<NCW, CPS, PAIR, S16, ZP, 4, ASM>;
   return nullptr;
 }
 
-template <int CPS, bool PAIR>
+template <int CPS, bool PAIR, bool ASM>
 MmaKernel pick(bool s16, bool zp, int cpg) {
-  if (s16) return zp ? pick_cpg<CPS, PAIR, true, true>(cpg) : pick_cpg<CPS, PAIR, true, false>(cpg);
-  return zp ? pick_cpg<CPS, PAIR, false, true>(cpg) : pick_cpg<CPS, PAIR, false, false>(cpg);
+  if (s16) return zp ? pick_cpg<CPS, PAIR, true, true, ASM>(cpg) : pick_cpg<CPS, PAIR, true, false, ASM>(cpg);
+  return zp ? pick_cpg<CPS, PAIR, false, true, ASM>(cpg) : pick_cpg<CPS, PAIR, false, false, ASM>(cpg);
 }
 
 // Dynamic shared memory per CTA when two CTAs share an SM, and when one CTA has the SM; the
@@ -442,6 +497,7 @@ constexpr int kOneBudget = 200 * 1024;
 constexpr int kStageTargetTwo = 40 * 1024;
 constexpr int kStageTargetOne = 72 * 1024;
 constexpr int kTwoMinStage = 32 * 1024;
+constexpr int kActSmemMax = 16 * 1024;  // activations staged in shared memory up to K = 8192
 
 template <bool PAIR>
 cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int K, int N, int bs, void* Y) {
@@ -467,7 +523,6 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   // A partial last tile copies nr * zrow zero-point bytes: a 16-byte multiple is required.
   if (zp && ((N % kRows) * a.zrow) % 16 != 0) return cudaErrorNotSupported;
   for (int t = 0; t < 2; ++t) a.zp[t] = w[t < NWT ? t : 0].zp;
-  const int act_bytes = K * 2;
   // Stage layout for a K slice of ks: [scale boxes][packed segments][zero points], 1024-aligned.
   auto layout = [&](int ks) {
     a.kslice = ks;
@@ -504,6 +559,10 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   // each stage also needs one tile-sum slot (plus one spare slot)
   const int rps_two = NWT * kNcwTwo * kRows * 4, rps_one = NWT * kNcwOne * kRows * 4;
   int grid = 0, cps = 0;
+  // The activation is staged in shared memory when it is small; larger ones are read
+  // through L1, leaving the shared memory to the weight stages.
+  a.act_smem = K * 2 <= kActSmemMax ? 1 : 0;
+  const int act_bytes = a.act_smem ? K * 2 : 0;
   const int avail = kTwoBudget - act_bytes - rps_two - 1024;
   for (int mult = 1; mult <= 2 && cps == 0; ++mult) {
     const int g = ctx.num_sms * mult < a.ntiles ? ctx.num_sms * mult : a.ntiles;
@@ -576,8 +635,8 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   }
   const int cpg = bs / 32;
   MmaKernel kern = nullptr;
-  if (cps == 2) kern = pick<2, PAIR>(s16, zp, cpg);
-  if (cps == 1) kern = pick<1, PAIR>(s16, zp, cpg);
+  if (cps == 2) kern = a.act_smem ? pick<2, PAIR, true>(s16, zp, cpg) : pick<2, PAIR, false>(s16, zp, cpg);
+  if (cps == 1) kern = a.act_smem ? pick<1, PAIR, true>(s16, zp, cpg) : pick<1, PAIR, false>(s16, zp, cpg);
   if (kern == nullptr) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
