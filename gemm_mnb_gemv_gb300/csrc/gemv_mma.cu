@@ -68,6 +68,10 @@ constexpr int kRows = 16;        // weight rows per tile (the MMA's M)
 constexpr int kBlockK = 256;     // k per block (8 chunks of 32): one 128-byte packed segment
 constexpr int kMaxStages = 8;
 constexpr int kBoxBytes = 2048;  // one swizzled box slab: 16 rows x 128 bytes
+// tile-sum floats per warp and weight in a slot: 32 lanes x 2 rows (one weight, posted per
+// lane), or the 16 rows (two weights, four lanes summed first)
+template <bool PAIR>
+constexpr int red_per_warp() { return PAIR ? kRows : 64; }
 
 struct MmaGemvArgs {
   const __half* A;
@@ -84,7 +88,7 @@ struct MmaGemvArgs {
   int stage_bytes;   // one stage: one weight's tile slice (multiple of 1024)
   int stages;
   int act_smem;      // 1: the activation is staged after the stages (K * 2 bytes), 0: read from L1/L2
-  int red_off;       // tile-sum slots after the stages (and the activation): [stages + 1][weights][warps][16]
+  int red_off;       // tile-sum slots after the stages (and the activation): [stages + 1][weights][warps][64]
   int ntiles;
   uint32_t* status;
   const __half* bias;
@@ -196,17 +200,27 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
       bulk_g2s(wb + p.zoff, (w1 ? p.zp[1] : p.zp[0]) + (long long)n0 * p.zrow, (uint32_t)(nr * p.zrow),
                &full_bar[slot]);
   };
-  // Adds the consumer warps' posted partials of tile tl (slot rp) in warp order and stores
-  // the tile's outputs (lanes 0..15).
-  auto store_tile = [&](int tl, const float* rp) {
+  // Adds the consumer warps' posted partials of tile tl (slot rp) in warp order (per lane:
+  // lanes 4r', 4r' + 1, 4r' + 2, 4r' + 3 of row r = r' + 8h in turn) and stores the tile's
+  // outputs (lanes 0..15).
+  auto store_tile = [&](int tl, const float* rp, bool per_lane) {
     const int n = (t_begin + tl) * kRows + lane;
     if (lane < kRows && n < p.N) {
       float v[NWT];
 #pragma unroll
       for (int w = 0; w < NWT; ++w) {
         float sum = 0.0f;
+        if (per_lane) {
+          const int gg = lane & 7, hh = lane >> 3;
 #pragma unroll
-        for (int ww = 0; ww < NCW; ++ww) sum += *(volatile const float*)&rp[(w * NCW + ww) * kRows + lane];
+          for (int ww = 0; ww < NCW; ++ww)
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt)
+              sum += *(volatile const float*)&rp[((w * NCW + ww) * 32 + 4 * gg + tt) * 2 + hh];
+        } else {
+#pragma unroll
+          for (int ww = 0; ww < NCW; ++ww) sum += *(volatile const float*)&rp[(w * NCW + ww) * kRows + lane];
+        }
         v[w] = sum;
       }
       __half out;
@@ -392,6 +406,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
     // the ring slot of a tile's last stage is released only after the post, so no warp can be
     // S + 1 tiles ahead of the warp that reads a slot.
     const bool deferred = ntl <= S + 1;
+    const bool ring = nst > S;  // stages reuse ring slots: the producer waits for them to empty
+    const bool per_lane = deferred && NWT == 1;
     int slot = 0;
     uint32_t phase = 0;
     for (int tl = 0; tl < ntl; ++tl) {
@@ -401,7 +417,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
       for (int wt = 0; wt < NWT; ++wt) {
         acc[wt][0] = acc[wt][1] = 0.0f;
         for (int si = 0; si < p.nslices; ++si) {
-          if (ok && !mbar_wait_bounded(&full_bar[slot], phase)) {
+          // (a phase that completed long ago is seen by test_wait without the try_wait round trip)
+          if (ok && !mbar_test_wait(&full_bar[slot], phase) && !mbar_wait_bounded(&full_bar[slot], phase)) {
             report_status(p.status, kStatusFullWait);
             atomicExch(&failed, 1);
             ok = false;
@@ -419,7 +436,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
           acc[wt][1] += v8;
           if (wt == NWT - 1 && si == p.nslices - 1) {
             last_slot = slot;
-          } else {
+          } else if (ring) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[slot]);  // this warp no longer reads the slot
           }
@@ -429,39 +446,47 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
           }
         }
       }
-      // Sum the four lanes of each row and post this warp's partials of the tile.
+      // Post this warp's partials of the tile: per lane for one weight when every tile has its
+      // own slot (they are added after the last tile), else the four lanes of each row summed
+      // first.
       const int rs = deferred ? tl : tl % (S + 1);
-      float* rp = red + (size_t)rs * (NWT * NCW * kRows);
+      float* rp = red + (size_t)rs * (NWT * NCW * red_per_warp<PAIR>());
+      if (per_lane) {
 #pragma unroll
-      for (int w = 0; w < NWT; ++w) {
+        for (int w = 0; w < NWT; ++w)
+          *reinterpret_cast<float2*>(&rp[((w * NCW + warp) * 32 + lane) * 2]) = make_float2(acc[w][0], acc[w][1]);
+      } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float x = acc[w][h];
-          x += __shfl_xor_sync(kFull, x, 1);
-          x += __shfl_xor_sync(kFull, x, 2);
-          if (t == 0) rp[(w * NCW + warp) * kRows + g + 8 * h] = x;
-        }
-      }
-      __syncwarp();
-      if (!deferred) {
-        unsigned last = 0;
-        if (lane == 0) {
-          __threadfence_block();
-          last = atomicInc(&red_cnt[rs], (unsigned)(NCW - 1)) == (unsigned)(NCW - 1);  // wraps to 0
-        }
-        last = __shfl_sync(kFull, last, 0);
-        if (last) {
-          __threadfence_block();
-          store_tile(tl, rp);
+        for (int w = 0; w < NWT; ++w) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float x = acc[w][h];
+            x += __shfl_xor_sync(kFull, x, 1);
+            x += __shfl_xor_sync(kFull, x, 2);
+            if (t == 0) rp[(w * NCW + warp) * kRows + g + 8 * h] = x;
+          }
         }
         __syncwarp();
+        if (!deferred) {
+          unsigned last = 0;
+          if (lane == 0) {
+            __threadfence_block();
+            last = atomicInc(&red_cnt[rs], (unsigned)(NCW - 1)) == (unsigned)(NCW - 1);  // wraps to 0
+          }
+          last = __shfl_sync(kFull, last, 0);
+          if (last) {
+            __threadfence_block();
+            store_tile(tl, rp, false);
+          }
+          __syncwarp();
+        }
       }
-      if (lane == 0) mbar_arrive(&empty_bar[last_slot]);
+      if (ring && lane == 0) mbar_arrive(&empty_bar[last_slot]);
     }
     if (deferred) {
       // every consumer warp has posted every tile: add and store them, one warp per tile
       asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
-      for (int tl = warp; tl < ntl; tl += NCW) store_tile(tl, red + (size_t)tl * (NWT * NCW * kRows));
+      for (int tl = warp; tl < ntl; tl += NCW) store_tile(tl, red + (size_t)tl * (NWT * NCW * red_per_warp<PAIR>()), per_lane);
     }
   }
 }
@@ -557,7 +582,7 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   //    (two stages in flight per CTA, sixteen warps computing per SM);
   //  * else one CTA per SM with sixteen consumer warps and a deeper ring.
   // each stage also needs one tile-sum slot (plus one spare slot)
-  const int rps_two = NWT * kNcwTwo * kRows * 4, rps_one = NWT * kNcwOne * kRows * 4;
+  const int rps_two = NWT * kNcwTwo * red_per_warp<PAIR>() * 4, rps_one = NWT * kNcwOne * red_per_warp<PAIR>() * 4;
   int grid = 0, cps = 0;
   // The activation is staged in shared memory when it is small; larger ones are read
   // through L1, leaving the shared memory to the weight stages.
@@ -593,7 +618,7 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   const bool two = cps > 1;
   const int ncw = two ? kNcwTwo : kNcwOne;
   a.red_off = a.stages * a.stage_bytes + act_bytes;
-  const size_t smem = (size_t)a.red_off + (size_t)(a.stages + 1) * NWT * ncw * kRows * 4 + 1024;
+  const size_t smem = (size_t)a.red_off + (size_t)(a.stages + 1) * NWT * ncw * red_per_warp<PAIR>() * 4 + 1024;
   a.status = ctx.status;
   a.bias = static_cast<const __half*>(ctx.bias);
   a.bias_mode = PAIR ? 0 : ctx.bias_mode;
