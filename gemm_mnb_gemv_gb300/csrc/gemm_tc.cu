@@ -406,11 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tbase = tmem + b * 256u + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * 128);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tc::tmem_ld32(tbase + c * 32, v);
-          tc::tmem_wait_ld();
+          // accumulator columns at or past the MMA's N hold nothing (the condition is the same
+          // for the whole warp, as the collective TMEM load requires)
+          if (half * 128 + c * 32 < p.nmma) {
+            float v[32];
+            tc::tmem_ld32(tbase + c * 32, v);
+            tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], s, acc[c * 32 + i]);
+            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], s, acc[c * 32 + i]);
+          }
         }
         tc::fence_before_sync();
         __syncwarp();
