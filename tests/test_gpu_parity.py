@@ -98,6 +98,9 @@ GEMV_CASES = [
     ("gv_mma_bs128_multi", 4096, 3001, 128, "f16", True, "normal", "gemv_mma"),
     ("gv_mma_sliced_f32", 14336, 517, 32, "f32", False, "normal", "gemv_mma"),
     ("gv_mma_one_tile", 256, 16, 32, "f16", True, "normal", "gemv_mma"),
+    # more tiles per CTA than ring slots + 1: stages reuse slots and each tile is summed by
+    # the last warp to post it (two CTAs of the call per SM, 7 tiles each)
+    ("gv_mma_many_tiles", 4096, 32768, 32, "f16", True, "normal", "gemv_mma"),
 ]
 
 
@@ -160,7 +163,9 @@ def test_gate_up_swiglu_workload_full_size(env):
     # the tensor-core pair kernel: half-SM CTAs, zero points with a ragged tile, K slices
     (2048, 333, 64, "f32", False, "gemv_pair_swiglu_mma"),
     (4096, 1000, 128, "f16", True, "gemv_pair_swiglu_mma"),
-    (14336, 100, 32, "f32", False, "gemv_pair_swiglu_mma")])
+    (14336, 100, 32, "f32", False, "gemv_pair_swiglu_mma"),
+    # more tiles per CTA than ring slots + 1 (the last warp to post a tile sums it)
+    (4096, 28672, 128, "f32", False, "gemv_pair_swiglu_mma")])
 def test_gate_up_swiglu_ragged(env, K, N, bs, sdt, zp, kernel):
     _swiglu_case(env, syn.custom(f"sw_{K}_{N}_{bs}", 1, K, N, bs, scales_dtype=sdt, has_zp=zp), kernel)
 
