@@ -228,8 +228,9 @@ size_t mnb_workspace_bytes(int M, int K, int N, int block_size) {
 
 namespace {
 
-// M = 1: GEMV; M > 16: tcgen05 GEMM on the repacked operand; otherwise the small-M
-// kernel.  Shapes no specialised kernel takes go to the generic kernel.
+// M = 1: GEMV; M > 16: tcgen05 GEMM on the repacked operand; otherwise the row mapping of
+// the GEMV kernel or the small-M kernel.  Shapes no specialised kernel takes go to the
+// generic kernel.
 cudaError_t dispatch_gemm(mnb::LaunchCtx& ctx, const void* A, int M, const mnb::QWeight& q,
                           const uint8_t* repacked, int K, int N, int bs, void* Y, void* workspace = nullptr,
                           size_t ws_bytes = 0) {
@@ -240,7 +241,10 @@ cudaError_t dispatch_gemm(mnb::LaunchCtx& ctx, const void* A, int M, const mnb::
     e = mnb::launch_gemm_tc(ctx, A, M, q, repacked, K, N, bs, Y, workspace, ws_bytes);
     if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, bs, Y);
   } else {
-    e = mnb::launch_gemm_smallm(ctx, A, M, q, K, N, bs, Y, workspace, ws_bytes);
+    // rows on the M = 1 kernel's machinery where its row mapping takes them (M <= 2 or 4 at
+    // block sizes 32 or 64), else the small-M kernel
+    e = mnb::launch_gemm_rows_mma(ctx, A, M, q, K, N, bs, Y);
+    if (e == cudaErrorNotSupported) e = mnb::launch_gemm_smallm(ctx, A, M, q, K, N, bs, Y, workspace, ws_bytes);
     if (e == cudaErrorNotSupported) e = mnb::launch_generic(ctx, A, M, q, K, N, bs, Y);
   }
   return e;

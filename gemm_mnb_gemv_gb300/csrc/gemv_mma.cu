@@ -75,6 +75,7 @@ constexpr int red_per_warp() { return PAIR ? kRows : 64; }
 
 struct MmaGemvArgs {
   const __half* A;
+  int M;             // activation rows (1: the GEMV mapping; 2 .. 2 * CPG: the row mapping)
   const uint8_t* zp[2];
   void* Y;
   int K, N;
@@ -100,6 +101,14 @@ struct MmaGemvArgs {
 struct BlockFrag {
   uint32_t w[4][16];
   float sa0, sa1, sb0, sb1;
+};
+
+// The row mapping's weight side of one block for one lane: the same 16 A-fragment words
+// (chunks t and t + 4) and the scales of its two D columns' groups: X row g, Y row g, X row
+// g + 8, Y row g + 8 (two each).
+struct RowFrag {
+  uint32_t w[4][16];
+  float s[8];
 };
 
 __device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
@@ -141,8 +150,9 @@ __device__ __forceinline__ void load_scales(uint32_t addr, float& s0, float& s1)
 
 // CPG: 32-k chunks per quant group (1, 2, 4 for block sizes 32, 64, 128).  CPS: CTAs that
 // share an SM (launch bounds leave each at most 1 / CPS of the registers).  ASM: the
-// activation is staged in shared memory.
-template <int NCW, int CPS, bool PAIR, bool S16, bool ZP, int CPG, bool ASM>
+// activation is staged in shared memory.  ROWS: 2 <= M <= 8 / G activation rows, G = 4 / CPG
+// quant groups in four chunks (the row mapping below; block sizes 32 and 64).
+template <int NCW, int CPS, bool PAIR, bool S16, bool ZP, int CPG, bool ASM, bool ROWS = false>
 __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
     gemv_mma_kernel(const MmaGemvArgs p, const __grid_constant__ CUtensorMap tmp0,
                     const __grid_constant__ CUtensorMap tmp1, const __grid_constant__ CUtensorMap tms0,
@@ -204,6 +214,25 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
   // lanes 4r', 4r' + 1, 4r' + 2, 4r' + 3 of row r = r' + 8h in turn) and stores the tile's
   // outputs (lanes 0..15).
   auto store_tile = [&](int tl, const float* rp, bool per_lane) {
+    if constexpr (ROWS) {
+      // output (m, r): lanes (r mod 8, t) of every warp whose columns 2t, 2t + 1 belong to row
+      // m, in warp then lane order
+      constexpr int G = 4 / CPG;
+      for (int o = lane; o < kRows * p.M; o += 32) {
+        const int r = o & (kRows - 1), m = o / kRows, n = (t_begin + tl) * kRows + r;
+        if (n >= p.N) continue;
+        float sum = 0.0f;
+#pragma unroll
+        for (int ww = 0; ww < NCW; ++ww)
+#pragma unroll
+          for (int tt = 0; tt < 4; ++tt)
+            if ((2 * tt) / G == m) sum += *(volatile const float*)&rp[(ww * 32 + 4 * (r & 7) + tt) * 2 + (r >> 3)];
+        __half out = round_out(sum, p.bias, n, p.bias_mode);
+        if (*(volatile int*)&failed) out = __ushort_as_half(0x7e00);
+        reinterpret_cast<__half*>(p.Y)[(long long)m * p.N + n] = out;
+      }
+      return;
+    }
     const int n = (t_begin + tl) * kRows + lane;
     if (lane < kRows && n < p.N) {
       float v[NWT];
@@ -358,8 +387,149 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
       v8 = fmaf(dy0[3] + dy1[3], f.sb1, v8);
     };
 
+    // Row mapping (ROWS): lane (g, t) converts chunks t (X) and t + 4 (Y) of rows g, g + 8, so
+    // one MMA's k range spans four consecutive chunks, G = 4 / CPG quant groups; B column
+    // m * G + j carries activation row m on the k slots of the chunks of group j (lanes t with
+    // t / CPG == j) and zeros elsewhere, so column m * G + j of D is each row's partial dot
+    // with row m over group j.  Lane (g, t) receives columns 2t, 2t + 1: activation row
+    // (2t) / G, groups (2t) mod G and the next.
+    constexpr int kG = 4 / CPG;
+    const int mb = g / kG;  // activation row of B column g
+    const uint32_t carrier = (uint32_t)(ROWS && g < p.M * kG && (t / CPG) == (g % kG));
+    const uint32_t bsw = (uint32_t)((mb & 1) << 2);
+    // zero-point bytes of chunks t, t + 4 of block b: rzx / rzy + rzs * b, nibble at rzsh
+    const int rzx = CPG == 1 ? (t >> 1) : 0, rzy = CPG == 1 ? 2 + (t >> 1) : 1, rzs = CPG == 1 ? 4 : 2;
+    const uint32_t rzsh = CPG == 1 ? 4u * (uint32_t)(t & 1) : 4u * (uint32_t)((t >> 1) & 1);
+    // scale bytes of the lane's two X groups and two Y groups of block b
+    const int rsx = (CPG == 1 ? 2 * (t & 1) : 0) * kSsz, rsy = rsx + (CPG == 1 ? 4 : 2) * kSsz;
+    const int rss = (CPG == 1 ? 8 : 4) * kSsz;
+    auto sw_off = [&](int o) -> uint32_t {  // swizzled offset of scale byte o (row g)
+      return (uint32_t)((o >> 7) * kBoxBytes + g * 128 + ((((o & 127) >> 4) ^ g) << 4) + (o & 15));
+    };
+    auto prep_rows = [&](uint32_t wbase, int b, RowFrag& f) {
+      const uint32_t seg = wbase + (uint32_t)(p.poff + b * kBoxBytes + g * 128);
+      const uint32_t rxa = seg + (uint32_t)((t ^ g) << 4), rya = seg + (uint32_t)(((t + 4) ^ g) << 4);
+      const uint4 xa = lds128_a(rxa), ya = lds128_a(rya);
+      const uint4 xb = lds128_a(rxa + 1024u), yb = lds128_a(rya + 1024u);
+      const uint32_t ox = sw_off(rsx + rss * b), oy = sw_off(rsy + rss * b);
+      load_scales<S16, 1>(wbase + ox, f.s[0], f.s[1]);
+      load_scales<S16, 1>(wbase + oy, f.s[2], f.s[3]);
+      load_scales<S16, 1>(wbase + ox + 1024u, f.s[4], f.s[5]);  // row g + 8: same swizzle
+      load_scales<S16, 1>(wbase + oy + 1024u, f.s[6], f.s[7]);
+      uint32_t zlxa = zl8, zhxa = zh8, zlya = zl8, zhya = zh8;
+      uint32_t zlxb = zl8, zhxb = zh8, zlyb = zl8, zhyb = zh8;
+      if constexpr (ZP) {
+        const uint32_t zrow = wbase + (uint32_t)(p.zoff + g * p.zrow + rzs * b);
+        const uint32_t zxa = (lds_u8_a(zrow + (uint32_t)rzx) >> rzsh) & 15u;
+        const uint32_t zya = (lds_u8_a(zrow + (uint32_t)rzy) >> rzsh) & 15u;
+        const uint32_t zxb = (lds_u8_a(zrow + (uint32_t)(rzx + 8 * p.zrow)) >> rzsh) & 15u;
+        const uint32_t zyb = (lds_u8_a(zrow + (uint32_t)(rzy + 8 * p.zrow)) >> rzsh) & 15u;
+        zlxa = zp_lo_const(zxa);
+        zhxa = zp_hi_const(zxa);
+        zlya = zp_lo_const(zya);
+        zhya = zp_hi_const(zya);
+        zlxb = zp_lo_const(zxb);
+        zhxb = zp_hi_const(zxb);
+        zlyb = zp_lo_const(zyb);
+        zhyb = zp_hi_const(zyb);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        nibbles_to_centered_half2(word_of(xa, q), zlxa, zhxa, f.w[q] + 0);
+        nibbles_to_centered_half2(word_of(xb, q), zlxb, zhxb, f.w[q] + 4);
+        nibbles_to_centered_half2(word_of(ya, q), zlya, zhya, f.w[q] + 8);
+        nibbles_to_centered_half2(word_of(yb, q), zlyb, zhyb, f.w[q] + 12);
+      }
+    };
+    // The staged activation of the row mapping: block kb, step q, row m, chunk c at 16-byte
+    // entry ((kb * 4 + q) * M + m) * 8 + (c ^ 4 (m mod 2)), the halves paired as the
+    // conversion pairs nibbles (the carriers of one step read distinct bank groups).
+    auto finish_rows = [&](int kb, const RowFrag& f, float& vg, float& v8) {
+      uint32_t bx[4][4], by[4][4];
+      const uint32_t base = act_u32 + (uint32_t)((kb * 4 * p.M + mb) * 8 * 16);
+      const uint32_t qs = (uint32_t)(p.M * 8 * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        bx[q][0] = bx[q][1] = bx[q][2] = bx[q][3] = 0u;
+        by[q][0] = by[q][1] = by[q][2] = by[q][3] = 0u;
+        lds128_pred(bx[q], base + q * qs + (((uint32_t)t ^ bsw) << 4), carrier);
+        lds128_pred(by[q], base + q * qs + (((uint32_t)(t + 4) ^ bsw) << 4), carrier);
+      }
+      float x0[4], x1[4], y0[4], y1[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t* da = f.w[q];
+        const uint32_t* db = f.w[q] + 4;
+        const uint32_t* ea = f.w[q] + 8;
+        const uint32_t* eb = f.w[q] + 12;
+        if (q == 0) {
+          mma16816_zero(x0, da[0], db[0], da[1], db[1], bx[q][0], bx[q][1]);
+          mma16816_zero(x1, da[2], db[2], da[3], db[3], bx[q][2], bx[q][3]);
+          mma16816_zero(y0, ea[0], eb[0], ea[1], eb[1], by[q][0], by[q][1]);
+          mma16816_zero(y1, ea[2], eb[2], ea[3], eb[3], by[q][2], by[q][3]);
+        } else {
+          mma16816(x0, da[0], db[0], da[1], db[1], bx[q][0], bx[q][1]);
+          mma16816(x1, da[2], db[2], da[3], db[3], bx[q][2], bx[q][3]);
+          mma16816(y0, ea[0], eb[0], ea[1], eb[1], by[q][0], by[q][1]);
+          mma16816(y1, ea[2], eb[2], ea[3], eb[3], by[q][2], by[q][3]);
+        }
+      }
+      // registers 0, 1: row g, columns 2t, 2t + 1; registers 2, 3: row g + 8
+      vg = fmaf(x0[0] + x1[0], f.s[0], vg);
+      vg = fmaf(x0[1] + x1[1], f.s[1], vg);
+      vg = fmaf(y0[0] + y1[0], f.s[2], vg);
+      vg = fmaf(y0[1] + y1[1], f.s[3], vg);
+      v8 = fmaf(x0[2] + x1[2], f.s[4], v8);
+      v8 = fmaf(x0[3] + x1[3], f.s[5], v8);
+      v8 = fmaf(y0[2] + y1[2], f.s[6], v8);
+      v8 = fmaf(y0[3] + y1[3], f.s[7], v8);
+    };
+
     pdl_wait();
-    if constexpr (ASM) {
+    if constexpr (ROWS) {
+      // Stage this warp's blocks of every activation row (lane l: halves 8l .. 8l + 7 of a
+      // block, chunk l / 4, step l % 4), up to eight (block, row) loads in flight per lane.
+      const int q = lane & 3, c = lane >> 2;
+      for (int si = 0; si < p.nslices; ++si) {
+        const int nb = (min(p.kslice, p.K - si * p.kslice)) / kBlockK;
+        const int b_lo = (warp * nb) / NCW, b_hi = ((warp + 1) * nb) / NCW;
+        // (block, row) pairs, row-minor, eight at a time: all loads, then all stores
+        for (int b0 = b_lo, m0 = 0; b0 < b_hi;) {
+          uint4 x[8];
+          int bb = b0, mm = m0;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            x[u] = make_uint4(0, 0, 0, 0);
+            if (bb < b_hi)
+              x[u] = *reinterpret_cast<const uint4*>(p.A + (long long)mm * p.K + (long long)(si * bps + bb) * kBlockK + 8 * lane);
+            if (++mm == p.M) {
+              mm = 0;
+              ++bb;
+            }
+          }
+          bb = b0;
+          mm = m0;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (bb < b_hi) {
+              uint32_t w4[4];
+              pair_halves_stride4(x[u], w4);
+              const int e = (((si * bps + bb) * 4 + q) * p.M + mm) * 8 + (c ^ ((mm & 1) << 2));
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(act_u32 + (uint32_t)(e * 16)), "r"(w4[0]),
+                           "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
+                           : "memory");
+            }
+            if (++mm == p.M) {
+              mm = 0;
+              ++bb;
+            }
+          }
+          b0 = bb;
+          m0 = mm;
+        }
+      }
+      __syncwarp();
+    } else if constexpr (ASM) {
       // Stage this warp's activation blocks in MMA order (lane l holds halves 8l .. 8l + 7 of
       // a block: chunk l / 4, step l % 4).
       for (int si = 0; si < p.nslices; ++si) {
@@ -428,9 +598,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
           const int b_lo = (warp * nb) / NCW, b_hi = ok ? ((warp + 1) * nb) / NCW : b_lo;
           float vg = 0.0f, v8 = 0.0f;  // this stage's partial sums of rows g and g + 8
           for (int b = b_lo; b < b_hi; ++b) {
-            BlockFrag f;
-            prep(wbase, b, f);
-            finish(si * bps + b, f, vg, v8);
+            if constexpr (ROWS) {
+              RowFrag f;
+              prep_rows(wbase, b, f);
+              finish_rows(si * bps + b, f, vg, v8);
+            } else {
+              BlockFrag f;
+              prep(wbase, b, f);
+              finish(si * bps + b, f, vg, v8);
+            }
           }
           acc[wt][0] += vg;
           acc[wt][1] += v8;
@@ -509,6 +685,20 @@ MmaKernel pick_cpg(int cpg) {
   return nullptr;
 }
 
+// The row mapping: two CTAs per SM, staged activations, block sizes 32 and 64.
+MmaKernel pick_rows(bool s16, bool zp, int cpg) {
+  constexpr int N8 = kNcwTwo;
+  if (cpg == 1) {
+    if (s16) return zp ? gemv_mma_kernel<N8, 2, false, true, true, 1, true, true> : gemv_mma_kernel<N8, 2, false, true, false, 1, true, true>;
+    return zp ? gemv_mma_kernel<N8, 2, false, false, true, 1, true, true> : gemv_mma_kernel<N8, 2, false, false, false, 1, true, true>;
+  }
+  if (cpg == 2) {
+    if (s16) return zp ? gemv_mma_kernel<N8, 2, false, true, true, 2, true, true> : gemv_mma_kernel<N8, 2, false, true, false, 2, true, true>;
+    return zp ? gemv_mma_kernel<N8, 2, false, false, true, 2, true, true> : gemv_mma_kernel<N8, 2, false, false, false, 2, true, true>;
+  }
+  return nullptr;
+}
+
 template <int CPS, bool PAIR, bool ASM>
 MmaKernel pick(bool s16, bool zp, int cpg) {
   if (s16) return zp ? pick_cpg<CPS, PAIR, true, true, ASM>(cpg) : pick_cpg<CPS, PAIR, true, false, ASM>(cpg);
@@ -523,11 +713,17 @@ constexpr int kStageTargetTwo = 40 * 1024;
 constexpr int kStageTargetOne = 72 * 1024;
 constexpr int kTwoMinStage = 32 * 1024;
 constexpr int kActSmemMax = 16 * 1024;  // activations staged in shared memory up to K = 8192
+constexpr int kTwoBudgetRows = 110 * 1024;   // the row mapping (its activation rows are larger)
+constexpr int kActSmemMaxRows = 32 * 1024;
 
-template <bool PAIR>
-cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int K, int N, int bs, void* Y) {
+// ROWS: 2 <= M <= 8 / G activation rows in the row mapping (M = 1 otherwise).
+template <bool PAIR, bool ROWS = false>
+cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int K, int N, int bs, void* Y,
+                            int M = 1) {
   constexpr int NWT = PAIR ? 2 : 1;
   if (K % kBlockK != 0 || (bs != 32 && bs != 64 && bs != 128) || K % bs != 0) return cudaErrorNotSupported;
+  if (ROWS && (PAIR || bs > 64 || M < 2 || M > 2 * (bs / 32) || (long long)M * K * 2 > kActSmemMaxRows))
+    return cudaErrorNotSupported;
   if (PAIR && (w[0].scales_f16 != w[1].scales_f16 || (w[0].zp == nullptr) != (w[1].zp == nullptr)))
     return cudaErrorNotSupported;
   auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
@@ -540,6 +736,7 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   if (srow % 16 != 0) return cudaErrorNotSupported;  // tensor-map row stride
   MmaGemvArgs a = {};
   a.A = static_cast<const __half*>(A);
+  a.M = ROWS ? M : 1;
   a.Y = Y;
   a.K = K;
   a.N = N;
@@ -586,9 +783,9 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   int grid = 0, cps = 0;
   // The activation is staged in shared memory when it is small; larger ones are read
   // through L1, leaving the shared memory to the weight stages.
-  a.act_smem = K * 2 <= kActSmemMax ? 1 : 0;
-  const int act_bytes = a.act_smem ? K * 2 : 0;
-  const int avail = kTwoBudget - act_bytes - rps_two - 1024;
+  a.act_smem = ROWS || K * 2 <= kActSmemMax ? 1 : 0;
+  const int act_bytes = a.act_smem ? a.M * K * 2 : 0;
+  const int avail = (ROWS ? kTwoBudgetRows : kTwoBudget) - act_bytes - rps_two - 1024;
   for (int mult = 1; mult <= 2 && cps == 0; ++mult) {
     const int g = ctx.num_sms * mult < a.ntiles ? ctx.num_sms * mult : a.ntiles;
     const int max_tiles = (a.ntiles + g - 1) / g;
@@ -607,6 +804,8 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
       }
     }
   }
+  if (ROWS && (cps != 2 || a.stages < (a.ntiles + grid - 1) / grid * a.nslices))
+    return cudaErrorNotSupported;  // the row mapping needs every tile of a CTA in flight
   if (cps == 0) {
     cps = 1;
     grid = ctx.num_sms < a.ntiles ? ctx.num_sms : a.ntiles;
@@ -660,12 +859,16 @@ cudaError_t launch_mma_impl(LaunchCtx& ctx, const void* A, const QWeight* w, int
   }
   const int cpg = bs / 32;
   MmaKernel kern = nullptr;
-  if (cps == 2) kern = a.act_smem ? pick<2, PAIR, true>(s16, zp, cpg) : pick<2, PAIR, false>(s16, zp, cpg);
-  if (cps == 1) kern = a.act_smem ? pick<1, PAIR, true>(s16, zp, cpg) : pick<1, PAIR, false>(s16, zp, cpg);
+  if (ROWS) {
+    kern = pick_rows(s16, zp, cpg);
+  } else {
+    if (cps == 2) kern = a.act_smem ? pick<2, PAIR, true>(s16, zp, cpg) : pick<2, PAIR, false>(s16, zp, cpg);
+    if (cps == 1) kern = a.act_smem ? pick<1, PAIR, true>(s16, zp, cpg) : pick<1, PAIR, false>(s16, zp, cpg);
+  }
   if (kern == nullptr) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ctx.variant = PAIR ? "gemv_pair_swiglu_mma" : "gemv_mma";
+  ctx.variant = PAIR ? "gemv_pair_swiglu_mma" : (ROWS ? "gemm_rows_mma" : "gemv_mma");
   const int threads = (ncw + 1) * 32;
   return launch_kernel(ctx, kern, dim3(grid), dim3(threads), smem, a, tp[0], tp[1], ts[0], ts[1]);
 }
@@ -680,6 +883,11 @@ cudaError_t launch_gemv_pair_swiglu_mma(LaunchCtx& ctx, const void* A, const QWe
                                         int K, int N, int bs, void* out) {
   const QWeight w[2] = {gate, up};
   return launch_mma_impl<true>(ctx, A, w, K, N, bs, out);
+}
+
+cudaError_t launch_gemm_rows_mma(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
+                                 void* Y) {
+  return launch_mma_impl<false, true>(ctx, A, &w, K, N, bs, Y, M);
 }
 
 }  // namespace mnb

@@ -52,6 +52,10 @@ cudaError_t launch_gemv_pair_swiglu_tma(LaunchCtx& ctx, const void* A, const QWe
 cudaError_t launch_gemv_mma(LaunchCtx& ctx, const void* A, const QWeight& w, int K, int N, int bs, void* Y);
 cudaError_t launch_gemv_pair_swiglu_mma(LaunchCtx& ctx, const void* A, const QWeight& gate, const QWeight& up,
                                         int K, int N, int bs, void* out);
+// 2 <= M <= 2 * (bs / 32) (block sizes 32 and 64, K % 256 == 0, M * K * 2 <= 32 KB) on the
+// M = 1 kernel's machinery with the row mapping; cudaErrorNotSupported otherwise.
+cudaError_t launch_gemm_rows_mma(LaunchCtx& ctx, const void* A, int M, const QWeight& w, int K, int N, int bs,
+                                 void* Y);
 // One-thread kernel whose bounded wait on a never-armed mbarrier gives up after limit_ns.
 cudaError_t launch_wait_selftest(LaunchCtx& ctx, uint64_t limit_ns);
 // Register-pipelined M = 1 GEMV; cudaErrorNotSupported when the shape has no variant.

@@ -119,6 +119,39 @@ def test_gemv_parity(env, name, K, N, bs, sdt, zp, act, kernel):
         assert variant == kernel or (kernel == "generic" and variant.startswith("generic")), variant
 
 
+def rows_mapping_takes(M, K, bs):
+    """Shapes the row mapping of the GEMV kernel takes (M <= 2 at block size 32, <= 4 at 64)."""
+    return bs in (32, 64) and 2 <= M <= 2 * (bs // 32) and K % 256 == 0 and M * K * 2 <= 32768
+
+
+# The row mapping: both block sizes, every M it takes, ragged N, fp32 scales, no zero points
+# with K slices, a single tile, and more tiles than fit two CTAs per SM (small-M kernel).
+ROWS_CASES = [
+    (2, 4096, 4096, 32, "f16", True, "gemm_rows_mma"),
+    (2, 1024, 333, 32, "f32", False, "gemm_rows_mma"),
+    (3, 2048, 1000, 64, "f16", True, "gemm_rows_mma"),
+    (4, 4096, 517, 64, "f32", True, "gemm_rows_mma"),
+    (2, 8192, 700, 64, "f16", False, "gemm_rows_mma"),   # whole-K stage too large: K slices
+    (4, 512, 16, 64, "f16", True, "gemm_rows_mma"),      # one tile, two blocks
+    (4, 4096, 14336, 64, "f16", True, "gemm_smallm_mma16816"),  # 6 tiles per CTA: small-M kernel
+    (3, 4096, 300, 32, "f16", True, "gemm_smallm_mma16816"),    # M > 2 at block size 32
+]
+
+
+@pytest.mark.parametrize("M,K,N,bs,sdt,zp,kernel", ROWS_CASES)
+def test_gemm_rows_mapping(env, M, K, N, bs, sdt, zp, kernel):
+    mnb, torch, dev = env
+    wl = syn.custom(f"rows_{M}_{K}_{N}_{bs}_{sdt}_{zp}", M, K, N, bs, scales_dtype=sdt, has_zp=zp)
+    w = syn.make_weight(wl)
+    A = syn.make_activation(wl)
+    y = mnb.mnb_gemm(upload_act(A, dev), *upload_weight(w, dev), K, N, bs)
+    assert mnb.mnb_last_variant() == kernel
+    torch.cuda.synchronize()
+    mnb.mnb_check_device_status()
+    Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
+    assert_within_bound(y.cpu().numpy(), Y, B, wl.name)
+
+
 @pytest.mark.parametrize("wname", ["tiny_gemv_k256_n128", "gemv_attnproj_k4096_n4096",
                                    "mlp_down_k14336_n4096"])
 def test_gemv_workloads_full_size(env, wname):
@@ -177,7 +210,8 @@ def test_gemm_small_m_workloads_full_size(env, M):
     w = syn.make_weight(wl)
     A = syn.make_activation(wl)
     y = mnb.mnb_gemm(upload_act(A, dev), *upload_weight(w, dev), wl.K, wl.N, wl.block_size)
-    assert mnb.mnb_last_variant() == "gemm_smallm_mma16816"
+    # M <= 4 at block size 64: the row mapping of the GEMV kernel; larger M: the small-M kernel
+    assert mnb.mnb_last_variant() == ("gemm_rows_mma" if M <= 4 else "gemm_smallm_mma16816")
     torch.cuda.synchronize()
     mnb.mnb_check_device_status()
     Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, wl.K, wl.N, wl.block_size)
@@ -218,7 +252,8 @@ def test_gemm_small_m_block_sizes(env, M, K, N, bs, sdt, zp):
     w = syn.make_weight(wl)
     A = syn.make_activation(wl)
     y = mnb.mnb_gemm(upload_act(A, dev), *upload_weight(w, dev), K, N, bs)
-    assert mnb.mnb_last_variant() == "gemm_smallm_mma16816"
+    expected = "gemm_rows_mma" if rows_mapping_takes(M, K, bs) else "gemm_smallm_mma16816"
+    assert mnb.mnb_last_variant() == expected
     torch.cuda.synchronize()
     mnb.mnb_check_device_status()
     Y, B = orc.matmul(A, w.packed, w.scales, w.zero_points, K, N, bs)
@@ -325,21 +360,26 @@ def test_graph_capture_replay_matches_eager(env):
     wt = upload_weight(w, dev)
     a = upload_act(A, dev)
     y1 = torch.empty(wl.N, dtype=torch.float16, device=dev)
+    y2 = torch.empty((2, wl.N), dtype=torch.float16, device=dev)
     y4 = torch.empty((4, wl.N), dtype=torch.float16, device=dev)
-    e1 = mnb.mnb_gemv(a[0].contiguous(), *wt, wl.K, wl.N, wl.block_size).clone()
+    a0, a2 = a[0].contiguous(), a[:2].contiguous()
+    e1 = mnb.mnb_gemv(a0, *wt, wl.K, wl.N, wl.block_size).clone()
+    e2 = mnb.mnb_gemm(a2, *wt, wl.K, wl.N, wl.block_size).clone()
+    assert mnb.mnb_last_variant() == "gemm_rows_mma"
     e4 = mnb.mnb_gemm(a, *wt, wl.K, wl.N, wl.block_size).clone()
-    a0 = a[0].contiguous()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
             mnb.mnb_gemv(a0, *wt, wl.K, wl.N, wl.block_size, out=y1)
+            mnb.mnb_gemm(a2, *wt, wl.K, wl.N, wl.block_size, out=y2)
             mnb.mnb_gemm(a, *wt, wl.K, wl.N, wl.block_size, out=y4)
+            mnb.mnb_gemm(a2, *wt, wl.K, wl.N, wl.block_size, out=y2)
     torch.cuda.current_stream().wait_stream(s)
     g.replay()
     torch.cuda.synchronize()
-    assert torch.equal(y1, e1) and torch.equal(y4, e4)
+    assert torch.equal(y1, e1) and torch.equal(y2, e2) and torch.equal(y4, e4)
 
 
 # M > 16 with few output tiles: K split over the SMs (fp32 partials, summed in slice order).
@@ -565,7 +605,8 @@ BIAS_CASES = [  # (M, K, N, bs, expected variant prefix)
     (1, 2048, 300, 16, "gemv_tma_ring"),
     (1, 96, 130, 32, "gemv_f16acc32"),
     (1, 48, 33, 16, "generic"),
-    (4, 4096, 300, 64, "gemm_smallm"),
+    (4, 4096, 300, 64, "gemm_rows_mma"),
+    (8, 4096, 300, 64, "gemm_smallm"),
     (3, 96, 77, 16, "generic"),
     (64, 256, 300, 128, "gemm_tcgen05"),
     (40, 256, 100, 64, "gemm_tcgen05"),
