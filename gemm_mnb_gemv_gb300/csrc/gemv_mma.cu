@@ -37,11 +37,17 @@
 // stages keep the shared memory: each warp requests the lines of its blocks into L1, and
 // the 8 lanes that carry B load their chunk (64 contiguous bytes per block) and pair it.
 //
-// Tile sums.  After a tile each warp sums its four lanes per row and posts the partials of
-// its 16 rows.  When a CTA has at most S + 1 tiles (S ring stages) each tile has its own
-// slot and one warp per tile adds and stores the posted partials after a barrier of the
-// consumer warps at the end; otherwise the last warp to post a tile (a shared-memory
-// counter) adds and stores it, so no warp waits on the others.
+// Tile sums.  With one weight and at most S + 1 tiles per CTA (S ring stages), each lane
+// posts its two row partials of a tile to the tile's own slot and, after a barrier of the
+// consumer warps at the end, one warp per tile adds them in warp and lane order and stores
+// it; otherwise each warp sums its four lanes per row first and the last warp to post a
+// tile (a shared-memory counter) adds and stores it, so no warp waits on the others.
+//
+// Row mapping (speculative verify, 2 <= M <= 8 / G, G = 4 / CPG quant groups per four
+// chunks: block sizes 32 and 64).  Lane (g, t) converts chunks t and t + 4 instead, so one
+// MMA's k range spans four consecutive chunks; B column m * G + j carries activation row m
+// on the k slots of group j and zeros elsewhere, and D column m * G + j is each weight
+// row's partial dot with row m over group j: the same 16 MMAs per 4096 weights as M = 1.
 //
 // Launch overlap.  When a CTA's whole share fits half an SM (8 consumer warps, at most half
 // the SM's registers and shared memory each), one CTA per SM per call: the next call's CTA
