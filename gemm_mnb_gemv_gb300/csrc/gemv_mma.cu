@@ -102,10 +102,11 @@ struct MmaGemvArgs {
   int bias_mode;
 };
 
-// One block's weight side for one lane: A fragments of the 16 MMAs (per step q: X rows g,
-// g + 8, then Y rows g, g + 8, four registers each) and the scales of its two chunks.
+// One block's weight side for one lane: the packed words of chunks 2t (X) and 2t + 1 (Y) of
+// rows g (a) and g + 8 (b), the conversion constants of their zero points and the scales.
 struct BlockFrag {
-  uint32_t w[4][16];
+  uint4 xa, ya, xb, yb;
+  uint32_t zlxa, zhxa, zlya, zhya, zlxb, zhxb, zlyb, zhyb;
   float sa0, sa1, sb0, sb1;
 };
 
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
     const int sos = (CPG == 1 ? 8 : (CPG == 2 ? 4 : 2)) * kSsz;
     const uint32_t zl8 = zp_lo_const(8u), zh8 = zp_hi_const(8u);
     // Block b of the stage at wbase, weight side: rows g and g + 8, chunks 2t (X) and 2t + 1
-    // (Y), converted to the MMA's A fragments, and their scales.
+    // (Y), their zero points' conversion constants and their scales.
     auto prep = [&](uint32_t wbase, int b, BlockFrag& f) {
       const int o0 = so0 + sos * b;  // scale byte within the slice's boxes
       const uint32_t soff = (uint32_t)((o0 >> 7) * kBoxBytes + g * 128 + ((((o0 & 127) >> 4) ^ g) << 4) + (o0 & 15));
@@ -313,32 +314,27 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
       // 1024 bytes on, same swizzle
       const uint32_t seg = wbase + (uint32_t)(p.poff + b * kBoxBytes + g * 128);
       const uint32_t rxa = seg + (uint32_t)(((2 * t) ^ g) << 4), rya = seg + (uint32_t)(((2 * t + 1) ^ g) << 4);
-      const uint4 xa = lds128_a(rxa), ya = lds128_a(rya);
-      const uint4 xb = lds128_a(rxa + 1024u), yb = lds128_a(rya + 1024u);
+      f.xa = lds128_a(rxa);
+      f.ya = lds128_a(rya);
+      f.xb = lds128_a(rxa + 1024u);
+      f.yb = lds128_a(rya + 1024u);
       load_scales<S16, CPG>(wbase + soff, f.sa0, f.sa1);
       load_scales<S16, CPG>(wbase + soff + 1024u, f.sb0, f.sb1);  // row g + 8: same swizzle
-      uint32_t zlxa = zl8, zhxa = zh8, zlya = zl8, zhya = zh8;
-      uint32_t zlxb = zl8, zhxb = zh8, zlyb = zl8, zhyb = zh8;
+      f.zlxa = f.zlya = f.zlxb = f.zlyb = zl8;
+      f.zhxa = f.zhya = f.zhxb = f.zhyb = zh8;
       if constexpr (ZP) {
         const uint32_t zaddr = wbase + (uint32_t)(p.zoff + g * p.zrow + zb0 + zbs * b);
         const uint32_t za = lds_u8_a(zaddr), zb = lds_u8_a(zaddr + (uint32_t)(8 * p.zrow));
         const uint32_t za0 = (za >> zsh0) & 15u, za1 = (za >> zsh1) & 15u;
         const uint32_t zb0v = (zb >> zsh0) & 15u, zb1v = (zb >> zsh1) & 15u;
-        zlxa = zp_lo_const(za0);
-        zhxa = zp_hi_const(za0);
-        zlya = zp_lo_const(za1);
-        zhya = zp_hi_const(za1);
-        zlxb = zp_lo_const(zb0v);
-        zhxb = zp_hi_const(zb0v);
-        zlyb = zp_lo_const(zb1v);
-        zhyb = zp_hi_const(zb1v);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        nibbles_to_centered_half2(word_of(xa, q), zlxa, zhxa, f.w[q] + 0);
-        nibbles_to_centered_half2(word_of(xb, q), zlxb, zhxb, f.w[q] + 4);
-        nibbles_to_centered_half2(word_of(ya, q), zlya, zhya, f.w[q] + 8);
-        nibbles_to_centered_half2(word_of(yb, q), zlyb, zhyb, f.w[q] + 12);
+        f.zlxa = zp_lo_const(za0);
+        f.zhxa = zp_hi_const(za0);
+        f.zlya = zp_lo_const(za1);
+        f.zhya = zp_hi_const(za1);
+        f.zlxb = zp_lo_const(zb0v);
+        f.zhxb = zp_hi_const(zb0v);
+        f.zlyb = zp_lo_const(zb1v);
+        f.zhyb = zp_hi_const(zb1v);
       }
     };
     // The activation side of 256-k block kb and the MMAs; adds the scaled partial dots of
@@ -367,13 +363,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
 #pragma unroll
         for (int q = 0; q < 4; ++q) pair_halves_stride4(av[q], bq[q]);
       }
+      // step q: its four words converted to A fragments right before its four MMAs
       float dx0[4], dx1[4], dy0[4], dy1[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint32_t* da = f.w[q];
-        const uint32_t* db = f.w[q] + 4;
-        const uint32_t* ea = f.w[q] + 8;
-        const uint32_t* eb = f.w[q] + 12;
+        uint32_t da[4], db[4], ea[4], eb[4];
+        nibbles_to_centered_half2(word_of(f.xa, q), f.zlxa, f.zhxa, da);
+        nibbles_to_centered_half2(word_of(f.xb, q), f.zlxb, f.zhxb, db);
+        nibbles_to_centered_half2(word_of(f.ya, q), f.zlya, f.zhya, ea);
+        nibbles_to_centered_half2(word_of(f.yb, q), f.zlyb, f.zhyb, eb);
         if (q == 0) {
           mma16816_zero(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
           mma16816_zero(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
