@@ -363,8 +363,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
 #pragma unroll
         for (int q = 0; q < 4; ++q) pair_halves_stride4(av[q], bq[q]);
       }
-      // step q: its four words converted to A fragments right before its four MMAs
-      float dx0[4], dx1[4], dy0[4], dy1[4];
+      // step q: its four words converted to A fragments right before its four MMAs; one
+      // accumulator for the X MMAs and one for the Y MMAs (eight MMAs each per block)
+      float dx[4], dy[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t da[4], db[4], ea[4], eb[4];
@@ -373,22 +374,20 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS)
         nibbles_to_centered_half2(word_of(f.ya, q), f.zlya, f.zhya, ea);
         nibbles_to_centered_half2(word_of(f.yb, q), f.zlyb, f.zhyb, eb);
         if (q == 0) {
-          mma16816_zero(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
-          mma16816_zero(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
-          mma16816_zero(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
-          mma16816_zero(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
+          mma16816_zero(dx, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
+          mma16816_zero(dy, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
         } else {
-          mma16816(dx0, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
-          mma16816(dx1, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
-          mma16816(dy0, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
-          mma16816(dy1, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
+          mma16816(dx, da[0], db[0], da[1], db[1], bq[q][0], bq[q][1]);
+          mma16816(dy, ea[0], eb[0], ea[1], eb[1], bq[q][0], bq[q][1]);
         }
+        mma16816(dx, da[2], db[2], da[3], db[3], bq[q][2], bq[q][3]);
+        mma16816(dy, ea[2], eb[2], ea[3], eb[3], bq[q][2], bq[q][3]);
       }
       // lane (g, t): X column 2t (registers 0, 2) and Y column 2t + 1 (registers 1, 3)
-      vg = fmaf(dx0[0] + dx1[0], f.sa0, vg);
-      vg = fmaf(dy0[1] + dy1[1], f.sa1, vg);
-      v8 = fmaf(dx0[2] + dx1[2], f.sb0, v8);
-      v8 = fmaf(dy0[3] + dy1[3], f.sb1, v8);
+      vg = fmaf(dx[0], f.sa0, vg);
+      vg = fmaf(dy[1], f.sa1, vg);
+      v8 = fmaf(dx[2], f.sb0, v8);
+      v8 = fmaf(dy[3], f.sb1, v8);
     };
 
     // Row mapping (ROWS): lane (g, t) converts chunks t (X) and t + 4 (Y) of rows g, g + 8, so
